@@ -1,0 +1,326 @@
+"""Pins for the oracle's fused epilogue, quantisers, R-way sum and workspace
+arithmetic.  Every expected value here comes from something other than the
+oracle's own formula: a closed form, a special case that reduces to a library
+routine (torch bf16 arithmetic, torch rms_norm), exact rational arithmetic on
+tiny inputs, an invariant, or a worked value stated in the test.
+
+Sources of the definitions (page title, function):
+  TensorRT-LLM allReduceFusionKernels.cu: allreduce_sum (fp32 rank-order
+    accumulation, one rounding), add128 / fused_op (residual add in the element
+    type), rms_norm (acc / hidden_dim + eps, then x * s * gamma),
+    is_neg_zero / push loop of allreduce_fusion_kernel_oneshot_lamport
+    (-0.0 sentinel per 32-bit word), Workspace (region sizes).
+  mscclpp allreduce.cu: vectorSum (plain element-wise R-way sum).
+"""
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from allreduce_residual_rmsnorm_gb300 import workloads as W
+
+BF16 = oracle.BF16
+FP16 = oracle.FP16
+bits = W.bits
+
+
+def bf(x):
+    return torch.as_tensor(x, dtype=torch.float32).to(torch.bfloat16)
+
+
+def ulp_diff_bf16(a_bits, b_bits):
+    """Distance in bf16 ulps between two arrays of bf16 bit patterns (finite)."""
+    def key(b):
+        b = b.astype(np.int32)
+        return np.where(b & 0x8000, -(b & 0x7fff), b & 0x7fff)
+    return np.abs(key(a_bits) - key(b_bits))
+
+
+def run(partials, residual, gamma, eps, dtype=BF16):
+    return oracle.fused(dtype, bits(partials), bits(residual), bits(gamma), eps, threads=2)
+
+
+# -------------------------------------------------- residual path (steps 1-2)
+
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 8, 16])
+def test_identical_partials_sum_equals_R_times_x(R):
+    # R copies of x: every partial fp32 sum k*x has at most 12 significant
+    # bits, so the rank sum is exactly R*x and the only rounding is the final
+    # one -- the same as torch's single fp32 -> bf16 conversion of R*x.
+    g = torch.Generator().manual_seed(R)
+    T, H = 5, 72
+    x = torch.randn(T, H, generator=g).to(torch.bfloat16)
+    res = torch.randn(T, H, generator=g).to(torch.bfloat16)
+    gamma = (1 + 0.1 * torch.randn(H, generator=g)).to(torch.bfloat16)
+    partials = x.unsqueeze(0).expand(R, T, H).contiguous()
+    out, _, _ = run(partials, res, gamma, 1e-6)
+    a = (x.float() * R).to(torch.bfloat16)
+    expect = a + res        # torch CPU bf16 add: fp32 add, one RNE rounding
+    assert np.array_equal(out, bits(expect))
+
+
+def test_zero_partials_leave_residual_unchanged_and_norm_is_textbook():
+    g = torch.Generator().manual_seed(7)
+    R, T, H = 4, 6, 256
+    res = torch.randn(T, H, generator=g).to(torch.bfloat16)
+    gamma = (1 + 0.1 * torch.randn(H, generator=g)).to(torch.bfloat16)
+    partials = torch.zeros(R, T, H, dtype=torch.bfloat16)
+    out, nrm, _ = run(partials, res, gamma, 1e-6)
+    assert np.array_equal(out, bits(res))
+    ref = F.rms_norm(res.float(), (H,), gamma.float(), 1e-6).to(torch.bfloat16)
+    d = ulp_diff_bf16(nrm, bits(ref))
+    assert d.max() <= 1 and (d > 0).mean() < 0.01
+
+
+@pytest.mark.parametrize("dtype", [BF16, FP16])
+def test_single_rank_is_textbook_residual_rmsnorm(dtype):
+    tdt = torch.bfloat16 if dtype == BF16 else torch.float16
+    g = torch.Generator().manual_seed(11)
+    T, H = 8, 512
+    p = torch.randn(1, T, H, generator=g).to(tdt)
+    res = torch.randn(T, H, generator=g).to(tdt)
+    gamma = (1 + 0.1 * torch.randn(H, generator=g)).to(tdt)
+    out, nrm, _ = run(p, res, gamma, 1e-6, dtype)
+    y = p[0] + res          # torch CPU half/bf16 add: one rounding of the fp32 sum
+    assert np.array_equal(out, bits(y))
+    ref = F.rms_norm(y.float(), (H,), gamma.float(), 1e-6).to(tdt)
+    if dtype == BF16:
+        d = ulp_diff_bf16(nrm, bits(ref))
+    else:
+        d = np.abs(nrm.astype(np.int32) - bits(ref).astype(np.int32))
+    assert d.max() <= 1 and (d > 0).mean() < 0.01
+
+
+def test_rank_order_fp32_accumulation_worked_value():
+    # Partials 2^24, 1, -2^24 (all exact in bf16).  In fp32, rank order:
+    # 2^24 + 1 = 16777217 is not representable and rounds (tie, to even) to
+    # 2^24; adding -2^24 gives 0.  Any other order, or fp64, gives 1.
+    P = torch.zeros(3, 1, 8, dtype=torch.bfloat16)
+    P[0] = bf(2.0 ** 24)
+    P[1] = bf(1.0)
+    P[2] = bf(-(2.0 ** 24))
+    res = bf(np.full((1, 8), 0.5))
+    gamma = bf(np.ones(8))
+    out, _, _ = run(P, res, gamma, 1e-6)
+    assert np.array_equal(out, bits(res))                 # y = 0 + 0.5
+
+
+def test_rank_sum_is_rounded_before_residual_add_worked_value():
+    # s = 1 + 2^-8 is exactly half way between bf16 neighbours 1 and 1 + 2^-7:
+    # ties-to-even gives a = 1.  Then 1 + 2^-8 again rounds to 1.
+    # Adding the residual to the unrounded sum would give 1 + 2^-7 exactly.
+    P = torch.zeros(2, 1, 8, dtype=torch.bfloat16)
+    P[0] = bf(1.0)
+    P[1] = bf(2.0 ** -8)
+    res = bf(np.full((1, 8), 2.0 ** -8))
+    gamma = bf(np.ones(8))
+    out, _, _ = run(P, res, gamma, 1e-6)
+    assert np.array_equal(out, bits(bf(np.ones((1, 8)))))
+
+
+# ----------------------------------------------------- RMSNorm (steps 3-5)
+
+@pytest.mark.parametrize("H,c", [(8, 1.0), (512, -0.25), (7168, 4.0), (4096, -2.0 ** -6)])
+def test_constant_power_of_two_row_normalises_to_signed_gamma_exactly(H, c):
+    # y_h = c = +-2^k and eps = 0: ss = H c^2, ss / H = c^2, sqrt = |c|, all
+    # exact, so rstd = 1/|c| exactly and (c * rstd) * gamma = sign(c) * gamma.
+    g = torch.Generator().manual_seed(H)
+    gamma = (1 + 0.3 * torch.randn(H, generator=g)).to(torch.bfloat16)
+    P = torch.zeros(2, 1, H, dtype=torch.bfloat16)
+    res = bf(np.full((1, H), c))
+    _, nrm, rstd = run(P, res, gamma, 0.0)
+    assert rstd[0] == np.float32(1.0 / abs(c))
+    expect = gamma if c > 0 else -gamma
+    assert np.array_equal(nrm[0], bits(expect))
+
+
+def test_constant_row_with_eps_closed_form():
+    # rstd = 1 / sqrt(c^2 + eps): for c = 1 and eps = 0.5625 that is exactly
+    # 1 / 1.25 = 0.8 (rounded once to fp32), n = rnd((c*0.8f)*gamma).
+    H = 64
+    gamma = bf(np.linspace(-2, 2, H))
+    P = torch.zeros(1, 1, H, dtype=torch.bfloat16)
+    res = bf(np.ones((1, H)))
+    _, nrm, rstd = run(P, res, gamma, 0.5625)
+    assert rstd[0] == np.float32(0.8)
+    expect = (torch.full((H,), float(np.float32(0.8))) * gamma.float()).to(torch.bfloat16)
+    assert np.array_equal(nrm[0], bits(expect))
+
+
+def test_exact_rational_brute_force_tiny():
+    # Dyadic inputs (multiples of 1/16 in [-4, 4]) keep every fp32 rank sum and
+    # residual add exact, so y is one rounding of an exact rational.  ss, the
+    # mean, eps and the inverse square root are then done exactly / in fp64.
+    rng = np.random.default_rng(5)
+    for trial in range(20):
+        R = int(rng.integers(1, 5))
+        T = int(rng.integers(1, 4))
+        H = 8 * int(rng.integers(1, 5))
+        P = rng.integers(-64, 65, (R, T, H)) / 16.0
+        X = rng.integers(-64, 65, (T, H)) / 16.0
+        G = rng.integers(8, 24, H) / 16.0
+        eps = 1e-3
+        Pt, Xt, Gt = bf(P), bf(X), bf(G)
+        assert np.array_equal(Pt.float().numpy(), P) and np.array_equal(Xt.float().numpy(), X)
+        out, nrm, _ = run(Pt, Xt, Gt, eps)
+        for t in range(T):
+            s = [sum(Fraction(float(P[r, t, h])) for r in range(R)) for h in range(H)]
+            a = [float(bf(float(v))) for v in s]          # exact rational -> one rounding
+            y = [float(bf(ai + float(X[t, h]))) for h, ai in enumerate(a)]
+            assert np.array_equal(out[t], bits(bf(y)))
+            ss = sum(Fraction(v) ** 2 for v in y)
+            rstd = 1.0 / math.sqrt(float(ss / H) + eps)
+            n = bf([yi * rstd * float(G[h]) for h, yi in enumerate(y)])
+            d = ulp_diff_bf16(nrm[t], bits(n))
+            assert d.max() <= 1, (trial, t)
+
+
+def test_norm_invariant_locates_eps_and_mean():
+    # mean_h (n_h / gamma_h)^2 = ms / (ms + eps) up to bf16 rounding; a large
+    # eps makes the factor far from 1 so a misplaced eps or a wrong divisor
+    # for the mean shows up.
+    g = torch.Generator().manual_seed(3)
+    R, T, H = 3, 4, 1024
+    P = torch.randn(R, T, H, generator=g).to(torch.bfloat16)
+    X = torch.randn(T, H, generator=g).to(torch.bfloat16)
+    G = (1 + 0.1 * torch.randn(H, generator=g)).to(torch.bfloat16)
+    eps = 2.0
+    out, nrm, _ = run(P, X, G, eps)
+    y = torch.from_numpy(out.view(np.int16)).view(torch.bfloat16).double()
+    n = torch.from_numpy(nrm.view(np.int16)).view(torch.bfloat16).double()
+    ms = (y ** 2).mean(dim=1)
+    lhs = ((n / G.double()) ** 2).mean(dim=1)
+    rhs = ms / (ms + eps)
+    assert torch.allclose(lhs, rhs, rtol=6e-3)
+
+
+# ------------------------------------------------------- sentinel (staging)
+
+def test_lamport_flip_only_touches_negative_zero_words():
+    # little-endian pairs: (lo=+0, hi=-0) is the word 0x80000000 -> rewritten;
+    # (lo=-0, hi=+0) is 0x00008000 -> kept; other words kept.
+    a = np.array([0x0000, 0x8000, 0x8000, 0x0000, 0x8000, 0x8000, 0x3f80, 0x8000],
+                 dtype=np.uint16)
+    got = oracle.lamport_flip(a)
+    assert list(got) == [0x0000, 0x0000, 0x8000, 0x0000, 0x8000, 0x8000, 0x3f80, 0x8000]
+
+
+# ---------------------------------------------------------- FP8 per-tensor
+
+def _norm_of_random(T=16, H=256, seed=9):
+    g = torch.Generator().manual_seed(seed)
+    P = torch.randn(4, T, H, generator=g).to(torch.bfloat16)
+    X = torch.randn(T, H, generator=g).to(torch.bfloat16)
+    G = (1 + 0.1 * torch.randn(H, generator=g)).to(torch.bfloat16)
+    _, nrm, _ = run(P, X, G, 1e-6)
+    return nrm
+
+
+def test_fp8_amax_element_maps_to_448_and_roundtrip_bound():
+    nrm = _norm_of_random()
+    amax = oracle.amax(BF16, nrm)
+    n = torch.from_numpy(nrm.view(np.int16)).view(torch.bfloat16).float().numpy()
+    assert amax == np.abs(n).max()
+    inv = oracle.fp8_inv_scale(amax)
+    q = oracle.quant_fp8(BF16, nrm, inv)
+    at_max = np.abs(n) == amax
+    assert np.all((q[at_max] & 0x7f) == 0x7e)
+    scale = np.float32(amax / 448.0)
+    dq = oracle.e4m3_decode(q) * scale
+    normal = np.abs(n) * inv >= 2.0 ** -6
+    assert np.all(np.abs(dq - n)[normal] <= 2.0 ** -4 * np.abs(n)[normal] * (1 + 1e-6))
+    assert np.all(np.abs(dq - n)[~normal] <= 2.0 ** -10 * scale * (1 + 1e-6))
+    # sign and monotonicity
+    assert np.all(np.signbit(n[n != 0]) == ((q[n != 0] & 0x80) != 0))
+
+
+# ------------------------------------------------------------------ NVFP4
+
+def test_nvfp4_zero_block_and_max_element():
+    H = 64
+    n = np.zeros((2, H), np.uint16)
+    vals = np.linspace(-3, 5, 16)
+    n[0, 16:32] = bits(bf(vals))
+    n[1, 48:64] = bits(bf(-vals))
+    gs = oracle.nvfp4_global_scale(5.0)
+    q, s = oracle.quant_nvfp4(BF16, n, gs)
+    # all-zero blocks: scale 0 and every code 0
+    assert s[0, 0] == 0 and s[0, 2] == 0 and s[1, 0] == 0
+    assert np.all(q[0, 0:8] == 0) and np.all(q[1, 0:16] == 0)
+    # the element holding the block maximum encodes to +-6 (code 7 / 15)
+    codes0 = np.stack([q[0, 8:16] & 0xf, q[0, 8:16] >> 4], 1).ravel()
+    assert codes0[15] == 0x7
+    codes1 = np.stack([q[1, 24:32] & 0xf, q[1, 24:32] >> 4], 1).ravel()
+    assert codes1[15] == 0xf
+
+
+def test_nvfp4_nibble_order_convention():
+    # Stated convention: element 2k in the low nibble of byte k.
+    n = np.zeros((1, 16), np.uint16)
+    n[0, 0] = bits(bf(6.0)).item()       # first element large, second zero
+    gs = oracle.nvfp4_global_scale(6.0)
+    q, _ = oracle.quant_nvfp4(BF16, n, gs)
+    assert q[0, 0] == 0x07
+
+
+def test_nvfp4_roundtrip_bound_random():
+    nrm = _norm_of_random(T=32, H=512, seed=21)
+    amax = oracle.amax(BF16, nrm)
+    gs = oracle.nvfp4_global_scale(amax)
+    q, s = oracle.quant_nvfp4(BF16, nrm, gs)
+    n = torch.from_numpy(nrm.view(np.int16)).view(torch.bfloat16).float().numpy()
+    codes = np.stack([q & 0xf, q >> 4], -1).reshape(n.shape)
+    dec = oracle.e4m3_decode(s)                                   # [T, H/16]
+    dq = oracle.e2m1_decode(codes) * np.repeat(dec, 16, axis=1) / gs
+    err = np.abs(dq - n)
+    bmax = np.repeat(np.abs(n).reshape(n.shape[0], -1, 16).max(-1), 16, axis=1)
+    bound = np.repeat(dec, 16, axis=1) / gs + bmax * 2.0 ** -4
+    assert np.all(err <= bound * (1 + 1e-5))
+    # every block's maximum element encodes to +-6
+    blk = np.abs(n).reshape(n.shape[0], -1, 16)
+    cblk = codes.reshape(n.shape[0], -1, 16) & 0x7
+    arg = blk.argmax(-1)
+    top = np.take_along_axis(cblk, arg[..., None], -1)[..., 0]
+    nz = blk.max(-1) > 0
+    assert np.all(top[nz] == 7)
+
+
+# ------------------------------------------------------------- R-way sum
+
+def test_vector_sum_closed_form_and_fp64():
+    R, N = 8, 4099
+    ins = np.full((R, N), bits(torch.tensor([0.125], dtype=torch.float16)).item(), np.uint16)
+    out = oracle.vector_sum(FP16, ins, threads=2)
+    assert np.all(out == bits(torch.tensor([1.0], dtype=torch.float16)).item())   # 8 * 0.125
+    g = torch.Generator().manual_seed(0)
+    x = (torch.rand(R, N, generator=g) * 2 - 1).to(torch.float16)
+    out = oracle.vector_sum(FP16, bits(x), threads=2)
+    ref = x.double().sum(0).to(torch.float16)    # fp64 sum, one rounding (fp64->fp16)
+    mism = np.count_nonzero(out != bits(ref))
+    assert mism <= N // 1000, mism
+
+
+# ------------------------------------------------------ workspace / state
+
+def test_workspace_sizes_match_page_formula_golden():
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "workspace_sizes.txt")
+    rows = [ln.split() for ln in open(path) if ln.strip() and not ln.startswith("#")]
+    assert rows
+    for R, maxT, H, elem, oneshot, flags, buf, flg, slot, lam in rows:
+        got = oracle.workspace_sizes(int(R), int(maxT), int(H), int(elem), int(oneshot), int(flags))
+        assert got == (int(buf), int(flg), int(slot), int(lam))
+
+
+def test_lamport_state_cycles():
+    flag, clear = 0, 0
+    seen = []
+    for k in range(7):
+        flag, clear, rd, cl = oracle.lamport_step(flag, clear, 2, 16, 512)
+        seen.append((rd, cl, flag))
+        assert clear == 2 * 16 * 512
+    assert seen[:4] == [(0, 2, 1), (1, 0, 2), (2, 1, 0), (0, 2, 1)]

@@ -1,0 +1,112 @@
+"""The pins must catch plausible mistakes in the oracle.
+
+Each case plants one mistake in a copy of the oracle's C source (a dropped
+term, a wrong sign or index, a transposed operand, a wrong rounding rule),
+compiles it on the CPU, swaps it in, and checks that at least one pin fails.
+The committed oracle is untouched.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import oracle.oracle as OM
+import test_oracle_codecs as C
+import test_oracle_fused as Fz
+
+SRC = os.path.join(os.path.dirname(OM.__file__), "ar_oracle.c")
+
+MUTANTS = {
+    "drop_residual": ("dec_d(dtype, a) + dec_d(dtype, residual_in[t * H + h]));\n            if (residual_out)",
+                      "dec_d(dtype, a) + 0.0f);\n            if (residual_out)"),
+    "skip_last_rank": ("for (int r = 1; r < R; ++r)\n                s = s + dec_d(dtype, partials[(int64_t)r * rank_stride + t * H + h]);\n            uint16_t a = rnd_d(dtype, s);\n            uint16_t y = rnd_d(dtype, dec_d(dtype, a) + dec_d(dtype, residual_in[t * H + h]));\n            if (residual_out)",
+                       "for (int r = 1; r < R - 1; ++r)\n                s = s + dec_d(dtype, partials[(int64_t)r * rank_stride + t * H + h]);\n            uint16_t a = rnd_d(dtype, s);\n            uint16_t y = rnd_d(dtype, dec_d(dtype, a) + dec_d(dtype, residual_in[t * H + h]));\n            if (residual_out)"),
+    "subtract_rank": ("s = s + dec_d(dtype, partials[(int64_t)r * rank_stride + t * H + h]);\n            uint16_t a = rnd_d(dtype, s);\n            uint16_t y = rnd_d(dtype, dec_d(dtype, a) + dec_d(dtype, residual_in[t * H + h]));\n            if (residual_out)",
+                      "s = s - dec_d(dtype, partials[(int64_t)r * rank_stride + t * H + h]);\n            uint16_t a = rnd_d(dtype, s);\n            uint16_t y = rnd_d(dtype, dec_d(dtype, a) + dec_d(dtype, residual_in[t * H + h]));\n            if (residual_out)"),
+    "no_sum_rounding": ("uint16_t y = rnd_d(dtype, dec_d(dtype, a) + dec_d(dtype, residual_in[t * H + h]));\n            if (residual_out)",
+                        "uint16_t y = rnd_d(dtype, s + dec_d(dtype, residual_in[t * H + h])); (void)a;\n            if (residual_out)"),
+    "fp64_rank_sum": ("float s = dec_d(dtype, partials[0 * rank_stride + t * H + h]);\n            for (int r = 1; r < R; ++r)\n                s = s + dec_d(dtype, partials[(int64_t)r * rank_stride + t * H + h]);\n            uint16_t a = rnd_d(dtype, s);\n            uint16_t y = rnd_d(dtype, dec_d(dtype, a) + dec_d(dtype, residual_in[t * H + h]));\n            if (residual_out)",
+                      "double sd = dec_d(dtype, partials[0 * rank_stride + t * H + h]);\n            for (int r = 1; r < R; ++r)\n                sd = sd + dec_d(dtype, partials[(int64_t)r * rank_stride + t * H + h]);\n            float s = (float)sd;\n            uint16_t a = rnd_d(dtype, s);\n            uint16_t y = rnd_d(dtype, dec_d(dtype, a) + dec_d(dtype, residual_in[t * H + h]));\n            if (residual_out)"),
+    "mean_over_H_minus_1": ("float ms = ss32 / (float)H;", "float ms = ss32 / (float)(H - 1);"),
+    "eps_dropped": ("float v = ms + eps;", "float v = ms;"),
+    "eps_outside_sqrt": ("float v = ms + eps;\n        float rstd = 1.0f / sqrtf(v);",
+                         "float v = ms;\n        float rstd = 1.0f / (sqrtf(v) + eps);"),
+    "gamma_reversed": ("float n = ny * dec_d(dtype, gamma[h]);", "float n = ny * dec_d(dtype, gamma[H - 1 - h]);"),
+    "norm_uses_unrounded_sum": ("float ny = dec_d(dtype, y) * rstd;", "float ny = (dec_d(dtype, a) + dec_d(dtype, residual_in[t * H + h])) * rstd;"),
+    "bf16_ties_away": ("if (dropped > 0x8000u || (dropped == 0x8000u && (kept & 1u)))",
+                       "if (dropped >= 0x8000u)"),
+    "f16_truncate": ("if (dropped > 0x1000u || (dropped == 0x1000u && (kept & 1u)))", "if (0)"),
+    "e4m3_ties_away": ("if (frac > 0.5f || (frac == 0.5f && (n & 1u)))\n        n += 1u;\n    if (e == -6",
+                       "if (frac >= 0.5f)\n        n += 1u;\n    if (e == -6"),
+    "e4m3_no_subnormal": ("e = -6;                                       /* subnormal band: step 2^-9 */",
+                          "e = -7;"),
+    "e4m3_saturate_low": ("return s | 0x7e;\n    int e;", "return s | 0x7d;\n    int e;"),
+    "e2m1_ties_away": ("if (frac > 0.5f || (frac == 0.5f && (n & 1u)))\n        n += 1u;\n    if (ax < 1.0f && n < 2u)",
+                       "if (frac >= 0.5f)\n        n += 1u;\n    if (ax < 1.0f && n < 2u)"),
+    "e2m1_saturate_low": ("return s | 0x7;\n    int e;", "return s | 0x6;\n    int e;"),
+    "nvfp4_no_div6": ("float per_block = bmax / 6.0f;", "float per_block = bmax;"),
+    "nvfp4_nibbles_swapped": ("(uint8_t)(lo | (hi << 4))", "(uint8_t)(hi | (lo << 4))"),
+    "nvfp4_enc_inverted": ("float enc = (dec == 0.0f) ? 0.0f : gs / dec;", "float enc = (dec == 0.0f) ? 0.0f : dec / gs;"),
+    "fp8_scale_not_inverted": ("return 1.0f / scale;", "return scale;"),
+    "flip_wrong_word": ("if (words[i] == 0x80000000u)", "if (words[i] == 0x00008000u)"),
+    "sum_skips_rank": ("for (int r = 1; r < R; ++r)\n            s = s + dec_d(dtype, in[(int64_t)r * rank_stride + i]);",
+                       "for (int r = 2; r < R; ++r)\n            s = s + dec_d(dtype, in[(int64_t)r * rank_stride + i]);"),
+    "lamport_clear_wrong_slot": ("io[3] = (flag + 2) % 3;", "io[3] = (flag + 1) % 3;"),
+    "buffer_size_missing_R": ("out[0] = (int64_t)R * max_tokens * H * elem_bytes;", "out[0] = max_tokens * H * elem_bytes;"),
+}
+
+PINS = [
+    C.test_bf16_round_matches_torch, C.test_f16_round_matches_numpy,
+    C.test_e4m3_encode_matches_torch_below_saturation, C.test_e4m3_saturates_and_keeps_nan,
+    C.test_e4m3_ties_to_even_examples,
+    C.test_e2m1_encode_brute_force, C.test_e2m1_ties_to_even_examples,
+    lambda: C.test_e2m1_saturation_and_sign(100.0, 0x7),
+    lambda: [Fz.test_identical_partials_sum_equals_R_times_x(R) for R in (2, 3, 8)],
+    Fz.test_zero_partials_leave_residual_unchanged_and_norm_is_textbook,
+    lambda: Fz.test_single_rank_is_textbook_residual_rmsnorm(oracle.BF16),
+    Fz.test_rank_order_fp32_accumulation_worked_value,
+    Fz.test_rank_sum_is_rounded_before_residual_add_worked_value,
+    lambda: Fz.test_constant_power_of_two_row_normalises_to_signed_gamma_exactly(512, -0.25),
+    Fz.test_constant_row_with_eps_closed_form,
+    Fz.test_exact_rational_brute_force_tiny,
+    Fz.test_norm_invariant_locates_eps_and_mean,
+    Fz.test_lamport_flip_only_touches_negative_zero_words,
+    Fz.test_fp8_amax_element_maps_to_448_and_roundtrip_bound,
+    Fz.test_nvfp4_zero_block_and_max_element,
+    Fz.test_nvfp4_nibble_order_convention,
+    Fz.test_nvfp4_roundtrip_bound_random,
+    Fz.test_vector_sum_closed_form_and_fp64,
+    Fz.test_workspace_sizes_match_page_formula_golden,
+    Fz.test_lamport_state_cycles,
+]
+
+
+def _build_mutant(tmp_path, name):
+    src = open(SRC).read()
+    old, new = MUTANTS[name]
+    assert src.count(old) == 1, f"mutation anchor for {name} not unique/present"
+    path = tmp_path / f"{name}.c"
+    path.write_text(src.replace(old, new))
+    so = tmp_path / f"{name}.so"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+                           "-fPIC", "-shared", str(path), "-o", str(so), "-lm"])
+    return OM.load_library(str(so))
+
+
+def test_pins_pass_on_committed_oracle():
+    for pin in PINS:
+        pin()
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path, monkeypatch):
+    mutant = _build_mutant(tmp_path, name)
+    monkeypatch.setattr(OM, "_lib", mutant)
+    caught = []
+    for pin in PINS:
+        try:
+            pin()
+        except AssertionError:
+            caught.append(getattr(pin, "__name__", "lambda"))
+    assert caught, f"no pin caught mutant {name}"
