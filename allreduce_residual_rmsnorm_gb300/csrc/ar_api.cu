@@ -1,0 +1,647 @@
+// C ABI of libarfusion: workspace life cycle, staging, argument checks and
+// kernel dispatch.  Declarations and the contract of every entry point are in
+// include/ar_fusion.h.
+//
+// Workspace layout (TensorRT-LLM allReduceFusionKernels.cu, Workspace; the
+// FlashInfer workspace note), one device allocation, each region 256-byte
+// aligned:
+//   [buffer  R * maxT * H * elem]  rank r at r * maxT * H elements
+//   [flags   R * AR_BARRIER_FLAG_COUNT * 4]  reserved (zero)
+//   [lamport 3 slots of R * max(oneshot, maxT) * H * elem], -0.0f words when idle;
+//            within the slot, rank r at r * tokens * H elements of the call
+//   [state   struct ar_fusion_state]
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <new>
+#include <string>
+
+#include "ar_common.cuh"
+#include "ar_internal.h"
+
+namespace arf {
+cudaError_t launch_fused_rows_bf16(int variant, const FusedArgs& a, const LaunchCfg& c);
+cudaError_t launch_fused_rows_fp16(int variant, const FusedArgs& a, const LaunchCfg& c);
+
+cudaError_t launch_fused_rows(int dtype, int variant, const FusedArgs& a, const LaunchCfg& c)
+{
+    return dtype == AR_DT_BF16 ? launch_fused_rows_bf16(variant, a, c)
+                               : launch_fused_rows_fp16(variant, a, c);
+}
+}  // namespace arf
+
+using namespace arf;
+
+struct ar_fusion_ws {
+    int R, maxT, H, dtype;
+    int device, sms;
+    bool owned;
+    uint8_t* base;
+    uint64_t total, buffer_off, buffer_bytes, flag_off, flag_bytes, lamport_off, slot_bytes,
+        state_off;
+    int variant, mode, last_variant;
+    uint64_t timeout_ns;
+};
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what)
+{
+    return fail(AR_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+inline uint64_t align256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
+inline bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
+struct Layout {
+    uint64_t buffer_off, buffer_bytes, flag_off, flag_bytes, lamport_off, slot_bytes, state_off,
+        total;
+};
+
+Layout layout_of(int R, int maxT, int H)
+{
+    Layout L;
+    const uint64_t elem = 2;
+    const uint64_t tok = (uint64_t)(maxT > AR_ONESHOT_MAX_TOKENS ? maxT : AR_ONESHOT_MAX_TOKENS);
+    L.buffer_off = 0;
+    L.buffer_bytes = (uint64_t)R * maxT * H * elem;
+    L.flag_off = align256(L.buffer_off + L.buffer_bytes);
+    L.flag_bytes = (uint64_t)R * AR_BARRIER_FLAG_COUNT * 4;
+    L.lamport_off = align256(L.flag_off + L.flag_bytes);
+    L.slot_bytes = (uint64_t)R * tok * H * elem;
+    L.state_off = align256(L.lamport_off + 3 * L.slot_bytes);
+    L.total = align256(L.state_off + sizeof(ar_fusion_state));
+    return L;
+}
+
+int check_shape(int tp_size, int max_token_num, int hidden_dim, int dtype)
+{
+    if (dtype != AR_DT_BF16 && dtype != AR_DT_FP16)
+        return fail(AR_ERR_UNSUPPORTED, "dtype %d is not bf16 (0) or fp16 (1)", dtype);
+    if (tp_size < 1 || tp_size > AR_MAX_RANKS)
+        return fail(AR_ERR_UNSUPPORTED, "tp_size %d outside 1..%d", tp_size, AR_MAX_RANKS);
+    if (max_token_num < 1)
+        return fail(AR_ERR_INVALID, "max_token_num %d < 1", max_token_num);
+    if (hidden_dim <= 0 || hidden_dim % 8 != 0)
+        return fail(AR_ERR_INVALID, "hidden_dim %d is not a positive multiple of 8", hidden_dim);
+    if (hidden_dim > AR_MAX_HIDDEN)
+        return fail(AR_ERR_UNSUPPORTED, "hidden_dim %d > %d", hidden_dim, AR_MAX_HIDDEN);
+    return AR_OK;
+}
+
+// -------------------------------------------------------- small kernels
+
+__global__ void fill_u32_kernel(uint32_t* p, uint64_t n, uint32_t v)
+{
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
+        p[i] = v;
+}
+
+__global__ void init_state_kernel(ar_fusion_state* st, uint64_t comm_size)
+{
+    st->counter = 0;
+    st->flag = 0;
+    st->lamport_flag = 0;
+    st->pad0 = 0;
+    st->comm_size = comm_size;
+    st->clear_size = 0;
+    st->status = 0;
+    st->detail = -1;
+    st->calls = 0;
+}
+
+// Copy one rank's [T][H] partial into the workspace.  Lamport: into slot
+// (lamport_flag % 3) at rank * T * H elements, with every -0.0f word written as
+// +0.0f (the push loop of the one-shot kernel).  Buffer: plain copy.
+__global__ void stage_kernel(const uint4* src, uint8_t* region, uint64_t slot_bytes,
+                             uint64_t rank_off_bytes, uint64_t nvec, int lamport,
+                             const ar_fusion_state* st)
+{
+    uint8_t* dst = region + rank_off_bytes;
+    if (lamport) {
+        const uint32_t flag = *reinterpret_cast<const volatile uint32_t*>(&st->lamport_flag);
+        dst += (uint64_t)(flag % 3u) * slot_bytes;
+    }
+    uint4* d = reinterpret_cast<uint4*>(dst);
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+        uint4 v = ld_stream(src + i);
+        if (lamport) {
+            v.x = v.x == 0x80000000u ? 0u : v.x;
+            v.y = v.y == 0x80000000u ? 0u : v.y;
+            v.z = v.z == 0x80000000u ? 0u : v.z;
+            v.w = v.w == 0x80000000u ? 0u : v.w;
+        }
+        d[i] = v;
+    }
+}
+
+unsigned grid_for(uint64_t items, int threads, int sms)
+{
+    uint64_t b = (items + threads - 1) / threads;
+    const uint64_t cap = (uint64_t)sms * 16;
+    if (b > cap)
+        b = cap;
+    return b < 1 ? 1u : (unsigned)b;
+}
+
+int init_regions(ar_fusion_ws* ws, cudaStream_t s)
+{
+    cudaError_t e = cudaMemsetAsync(ws->base + ws->buffer_off, 0, ws->lamport_off, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaMemsetAsync(buffer, flags)");
+    const uint64_t words = 3 * ws->slot_bytes / 4;
+    fill_u32_kernel<<<grid_for(words, 256, ws->sms), 256, 0, s>>>(
+        reinterpret_cast<uint32_t*>(ws->base + ws->lamport_off), words, 0x80000000u);
+    init_state_kernel<<<1, 1, 0, s>>>(reinterpret_cast<ar_fusion_state*>(ws->base + ws->state_off),
+                                      ws->slot_bytes);
+    e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return cuda_fail(e, "workspace init kernels");
+    return AR_OK;
+}
+
+ar_fusion_state* state_of(ar_fusion_ws* ws)
+{
+    return reinterpret_cast<ar_fusion_state*>(ws->base + ws->state_off);
+}
+
+int resolve_mode(const ar_fusion_ws* ws, int mode, int tokens)
+{
+    if (mode == AR_MODE_AUTO)
+        mode = ws->mode;
+    if (mode == AR_MODE_AUTO)
+        mode = tokens <= AR_ONESHOT_MAX_TOKENS ? AR_MODE_LAMPORT : AR_MODE_BUFFER;
+    return mode;
+}
+
+bool valid_pattern(int p)
+{
+    const int q = p & (AR_QUANT_FP8 | AR_QUANT_NVFP4);
+    if (p & ~(AR_RESIDUAL_OUT | AR_NORM_OUT | AR_QUANT_FP8 | AR_QUANT_NVFP4))
+        return false;
+    if (q == (AR_QUANT_FP8 | AR_QUANT_NVFP4))
+        return false;
+    const int base = p & (AR_RESIDUAL_OUT | AR_NORM_OUT);
+    if (q)
+        return base == AR_RESIDUAL_OUT || base == (AR_RESIDUAL_OUT | AR_NORM_OUT);
+    return base == AR_NORM_OUT || base == (AR_RESIDUAL_OUT | AR_NORM_OUT);
+}
+
+// Common checks of ar_fusion_run / ar_fusion_norm_amax.  Fills `a` (pointers,
+// mode) on success.  `calib` = calibration pass (no outputs, no Lamport).
+int prepare(ar_fusion_ws* ws, const void* const* partials, int nranks, int tokens, int hidden,
+            int dtype, const void* residual_in, const void* gamma, float eps, int pattern,
+            void* residual_out, void* norm_out, void* quant_out, void* scale_out,
+            const float* scale_factor, bool calib, FusedArgs& a, bool& launch)
+{
+    launch = false;
+    if (!ws)
+        return fail(AR_ERR_INVALID, "workspace is NULL");
+    if (dtype != AR_DT_BF16 && dtype != AR_DT_FP16)
+        return fail(AR_ERR_UNSUPPORTED, "dtype %d is not bf16 (0) or fp16 (1)", dtype);
+    if (dtype != ws->dtype)
+        return fail(AR_ERR_INVALID, "dtype %d differs from the workspace's %d", dtype, ws->dtype);
+    if (nranks < 1 || nranks > AR_MAX_RANKS)
+        return fail(AR_ERR_UNSUPPORTED, "nranks %d outside 1..%d", nranks, AR_MAX_RANKS);
+    if (tokens < 0)
+        return fail(AR_ERR_INVALID, "tokens %d < 0", tokens);
+    if (hidden <= 0 || hidden % 8 != 0)
+        return fail(AR_ERR_INVALID, "hidden_dim %d is not a positive multiple of 8", hidden);
+    if (hidden > AR_MAX_HIDDEN)
+        return fail(AR_ERR_UNSUPPORTED, "hidden_dim %d > %d", hidden, AR_MAX_HIDDEN);
+    if (!calib) {
+        if (!valid_pattern(pattern))
+            return fail(AR_ERR_INVALID, "unsupported pattern 0x%x", pattern);
+        if ((pattern & AR_QUANT_NVFP4) && hidden % 16 != 0)
+            return fail(AR_ERR_INVALID, "NVFP4 needs hidden_dim %% 16 == 0 (got %d)", hidden);
+    }
+    const bool staged = partials == nullptr;
+    int mode = AR_MODE_BUFFER;
+    if (staged) {
+        if (nranks != ws->R)
+            return fail(AR_ERR_INVALID, "staged partials: nranks %d != tp_size %d", nranks, ws->R);
+        if (hidden != ws->H)
+            return fail(AR_ERR_INVALID, "staged partials: hidden %d != workspace hidden %d",
+                        hidden, ws->H);
+        if (tokens > ws->maxT)
+            return fail(AR_ERR_CAPACITY, "tokens %d > max_token_num %d", tokens, ws->maxT);
+        mode = calib ? AR_MODE_BUFFER : resolve_mode(ws, AR_MODE_AUTO, tokens);
+        if (mode != AR_MODE_LAMPORT && mode != AR_MODE_BUFFER)
+            return fail(AR_ERR_INVALID, "bad staged mode %d", mode);
+    }
+    if (tokens == 0)
+        return AR_OK;
+
+    // pointers
+    if (!residual_in || !gamma)
+        return fail(AR_ERR_INVALID, "residual_in and gamma must be non-NULL");
+    if (!aligned16(residual_in) || !aligned16(gamma))
+        return fail(AR_ERR_INVALID, "residual_in / gamma not 16-byte aligned");
+    if (!calib) {
+        if ((pattern & AR_RESIDUAL_OUT) && (!residual_out || !aligned16(residual_out)))
+            return fail(AR_ERR_INVALID, "residual_out NULL or not 16-byte aligned");
+        if ((pattern & AR_NORM_OUT) && (!norm_out || !aligned16(norm_out)))
+            return fail(AR_ERR_INVALID, "norm_out NULL or not 16-byte aligned");
+        if (pattern & (AR_QUANT_FP8 | AR_QUANT_NVFP4)) {
+            if (!quant_out || !aligned16(quant_out))
+                return fail(AR_ERR_INVALID, "quant_out NULL or not 16-byte aligned");
+            if (!scale_factor || ((uintptr_t)scale_factor & 3))
+                return fail(AR_ERR_INVALID, "scale_factor NULL or misaligned");
+        }
+        if ((pattern & AR_QUANT_NVFP4) && (!scale_out || !aligned16(scale_out)))
+            return fail(AR_ERR_INVALID, "scale_out NULL or not 16-byte aligned");
+    }
+
+    memset(&a, 0, sizeof a);
+    if (!staged) {
+        for (int r = 0; r < nranks; ++r) {
+            if (!partials[r] || !aligned16(partials[r]))
+                return fail(AR_ERR_INVALID, "partials[%d] NULL or not 16-byte aligned", r);
+            a.partial[r] = static_cast<const uint8_t*>(partials[r]);
+        }
+    } else if (mode == AR_MODE_BUFFER) {
+        for (int r = 0; r < nranks; ++r)
+            a.partial[r] = ws->base + ws->buffer_off + (uint64_t)r * ws->maxT * ws->H * 2;
+    } else {
+        a.lamport = 1;
+        a.lamport_base = ws->base + ws->lamport_off;
+        a.slot_bytes = ws->slot_bytes;
+    }
+    a.R = nranks;
+    a.T = tokens;
+    a.H = hidden;
+    a.pattern = calib ? 0 : pattern;
+    a.residual_in = static_cast<const uint8_t*>(residual_in);
+    a.gamma = static_cast<const uint8_t*>(gamma);
+    a.eps = eps;
+    if (!calib) {
+        a.residual_out = (pattern & AR_RESIDUAL_OUT) ? static_cast<uint8_t*>(residual_out) : nullptr;
+        a.norm_out = (pattern & AR_NORM_OUT) ? static_cast<uint8_t*>(norm_out) : nullptr;
+        a.quant_out = (pattern & (AR_QUANT_FP8 | AR_QUANT_NVFP4)) ? static_cast<uint8_t*>(quant_out)
+                                                                  : nullptr;
+        a.scale_out = (pattern & AR_QUANT_NVFP4) ? static_cast<uint8_t*>(scale_out) : nullptr;
+        a.scale_factor = (pattern & (AR_QUANT_FP8 | AR_QUANT_NVFP4)) ? scale_factor : nullptr;
+    }
+    a.state = state_of(ws);
+    a.timeout_ns = ws->timeout_ns;
+    launch = true;
+    return AR_OK;
+}
+
+int pick_variant(const ar_fusion_ws* ws, const FusedArgs& a)
+{
+    int v = ws->variant;
+    if (v == AR_VARIANT_BULK_PIPE && (a.lamport || !fused_pipe_supported(ws->dtype, a.H, a.R)))
+        v = AR_VARIANT_AUTO;
+    if (v == AR_VARIANT_WARP_ROW && a.H > 1024)
+        v = AR_VARIANT_AUTO;
+    if (v != AR_VARIANT_AUTO)
+        return v;
+    if (!a.lamport && fused_pipe_supported(ws->dtype, a.H, a.R) && a.T >= 2 * ws->sms)
+        return AR_VARIANT_BULK_PIPE;
+    return a.H <= 1024 ? AR_VARIANT_WARP_ROW : AR_VARIANT_CTA_ROW;
+}
+
+int launch_fused(ar_fusion_ws* ws, const FusedArgs& a, cudaStream_t s)
+{
+    const LaunchCfg c{ws->sms, s};
+    const int variant = pick_variant(ws, a);
+    ws->last_variant = variant;
+    cudaError_t e = variant == AR_VARIANT_BULK_PIPE ? launch_fused_pipe(ws->dtype, a, c)
+                                                    : launch_fused_rows(ws->dtype, variant, a, c);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "fused kernel launch");
+    return AR_OK;
+}
+
+}  // namespace
+
+// ======================================================================= ABI
+
+extern "C" {
+
+int ar_fusion_version(void) { return 10000; }
+
+const char* ar_fusion_last_error(void) { return g_err.c_str(); }
+
+int ar_fusion_workspace_bytes(int tp_size, int max_token_num, int hidden_dim, int dtype,
+                              size_t* bytes)
+{
+    if (!bytes)
+        return fail(AR_ERR_INVALID, "bytes is NULL");
+    int rc = check_shape(tp_size, max_token_num, hidden_dim, dtype);
+    if (rc)
+        return rc;
+    *bytes = (size_t)layout_of(tp_size, max_token_num, hidden_dim).total;
+    return AR_OK;
+}
+
+int ar_fusion_workspace_create(int tp_size, int max_token_num, int hidden_dim, int dtype,
+                               void* device_mem, size_t device_mem_bytes, void* stream,
+                               ar_fusion_ws** out)
+{
+    if (!out)
+        return fail(AR_ERR_INVALID, "out is NULL");
+    *out = nullptr;
+    int rc = check_shape(tp_size, max_token_num, hidden_dim, dtype);
+    if (rc)
+        return rc;
+    const Layout L = layout_of(tp_size, max_token_num, hidden_dim);
+    if (device_mem && (device_mem_bytes < L.total || ((uintptr_t)device_mem & 255)))
+        return fail(AR_ERR_INVALID, "device_mem too small (%zu < %llu) or not 256-byte aligned",
+                    device_mem_bytes, (unsigned long long)L.total);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaDeviceGetAttribute");
+    ar_fusion_ws* ws = new (std::nothrow) ar_fusion_ws();
+    if (!ws)
+        return fail(AR_ERR_INVALID, "out of host memory");
+    ws->R = tp_size;
+    ws->maxT = max_token_num;
+    ws->H = hidden_dim;
+    ws->dtype = dtype;
+    ws->device = dev;
+    ws->sms = sms;
+    ws->owned = device_mem == nullptr;
+    ws->total = L.total;
+    ws->buffer_off = L.buffer_off;
+    ws->buffer_bytes = L.buffer_bytes;
+    ws->flag_off = L.flag_off;
+    ws->flag_bytes = L.flag_bytes;
+    ws->lamport_off = L.lamport_off;
+    ws->slot_bytes = L.slot_bytes;
+    ws->state_off = L.state_off;
+    ws->variant = AR_VARIANT_AUTO;
+    ws->last_variant = AR_VARIANT_AUTO;
+    ws->mode = AR_MODE_AUTO;
+    ws->timeout_ns = 2000000000ull;
+    if (ws->owned) {
+        void* p = nullptr;
+        e = cudaMalloc(&p, L.total);
+        if (e != cudaSuccess) {
+            delete ws;
+            return cuda_fail(e, "cudaMalloc(workspace)");
+        }
+        ws->base = static_cast<uint8_t*>(p);
+    } else {
+        ws->base = static_cast<uint8_t*>(device_mem);
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    rc = init_regions(ws, s);
+    if (rc == AR_OK) {
+        e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess)
+            rc = cuda_fail(e, "cudaStreamSynchronize(create)");
+    }
+    if (rc != AR_OK) {
+        if (ws->owned)
+            cudaFree(ws->base);
+        delete ws;
+        return rc;
+    }
+    *out = ws;
+    return AR_OK;
+}
+
+int ar_fusion_workspace_destroy(ar_fusion_ws* ws)
+{
+    if (!ws)
+        return AR_OK;
+    int rc = AR_OK;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess)
+        rc = cuda_fail(e, "cudaDeviceSynchronize(destroy)");
+    if (ws->owned) {
+        e = cudaFree(ws->base);
+        if (e != cudaSuccess && rc == AR_OK)
+            rc = cuda_fail(e, "cudaFree(workspace)");
+    }
+    delete ws;
+    return rc;
+}
+
+int ar_fusion_workspace_info(const ar_fusion_ws* ws, ar_fusion_ws_info* info)
+{
+    if (!ws || !info)
+        return fail(AR_ERR_INVALID, "workspace or info is NULL");
+    memset(info, 0, sizeof *info);
+    info->tp_size = ws->R;
+    info->max_token_num = ws->maxT;
+    info->hidden_dim = ws->H;
+    info->dtype = ws->dtype;
+    info->elem_bytes = 2;
+    info->oneshot_max_tokens = AR_ONESHOT_MAX_TOKENS;
+    info->total_bytes = ws->total;
+    info->buffer_bytes = ws->buffer_bytes;
+    info->flag_bytes = ws->flag_bytes;
+    info->lamport_comm_bytes = ws->slot_bytes;
+    info->lamport_buffer_bytes = 3 * ws->slot_bytes;
+    info->state_bytes = sizeof(ar_fusion_state);
+    info->base = ws->base;
+    info->buffer = ws->base + ws->buffer_off;
+    info->flags = ws->base + ws->flag_off;
+    info->lamport = ws->base + ws->lamport_off;
+    info->state = ws->base + ws->state_off;
+    info->last_variant = ws->last_variant;
+    return AR_OK;
+}
+
+int ar_fusion_workspace_copy_state(ar_fusion_ws* ws, void* stream, ar_fusion_state* out)
+{
+    if (!ws || !out)
+        return fail(AR_ERR_INVALID, "workspace or out is NULL");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(out, state_of(ws), sizeof *out, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "reading workspace state");
+    return AR_OK;
+}
+
+int ar_fusion_workspace_status(ar_fusion_ws* ws, void* stream, int* detail)
+{
+    ar_fusion_state st;
+    int rc = ar_fusion_workspace_copy_state(ws, stream, &st);
+    if (rc)
+        return rc;
+    if (detail)
+        *detail = st.detail;
+    if (st.status != 0)
+        return fail(st.status, "device reported status %d (detail %d)", st.status, st.detail);
+    return AR_OK;
+}
+
+int ar_fusion_workspace_reset(ar_fusion_ws* ws, void* stream)
+{
+    if (!ws)
+        return fail(AR_ERR_INVALID, "workspace is NULL");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const uint64_t words = 3 * ws->slot_bytes / 4;
+    fill_u32_kernel<<<grid_for(words, 256, ws->sms), 256, 0, s>>>(
+        reinterpret_cast<uint32_t*>(ws->base + ws->lamport_off), words, 0x80000000u);
+    init_state_kernel<<<1, 1, 0, s>>>(state_of(ws), ws->slot_bytes);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return cuda_fail(e, "workspace reset kernels");
+    return AR_OK;
+}
+
+int ar_fusion_workspace_set_timeout_ns(ar_fusion_ws* ws, uint64_t ns)
+{
+    if (!ws || ns == 0)
+        return fail(AR_ERR_INVALID, "workspace NULL or timeout 0");
+    ws->timeout_ns = ns;
+    return AR_OK;
+}
+
+int ar_fusion_workspace_set_variant(ar_fusion_ws* ws, int variant)
+{
+    if (!ws || variant < AR_VARIANT_AUTO || variant > AR_VARIANT_BULK_PIPE)
+        return fail(AR_ERR_INVALID, "workspace NULL or variant %d unknown", variant);
+    ws->variant = variant;
+    return AR_OK;
+}
+
+int ar_fusion_workspace_set_mode(ar_fusion_ws* ws, int mode)
+{
+    if (!ws || mode < AR_MODE_AUTO || mode > AR_MODE_BUFFER)
+        return fail(AR_ERR_INVALID, "workspace NULL or mode %d unknown", mode);
+    ws->mode = mode;
+    return AR_OK;
+}
+
+int ar_fusion_workspace_stage(ar_fusion_ws* ws, int rank, const void* src, int tokens, int mode,
+                              void* stream)
+{
+    if (!ws)
+        return fail(AR_ERR_INVALID, "workspace is NULL");
+    if (rank < 0 || rank >= ws->R)
+        return fail(AR_ERR_INVALID, "rank %d outside 0..%d", rank, ws->R - 1);
+    if (mode < AR_MODE_AUTO || mode > AR_MODE_BUFFER)
+        return fail(AR_ERR_INVALID, "mode %d unknown", mode);
+    if (tokens < 0)
+        return fail(AR_ERR_INVALID, "tokens %d < 0", tokens);
+    if (tokens > ws->maxT)
+        return fail(AR_ERR_CAPACITY, "tokens %d > max_token_num %d", tokens, ws->maxT);
+    if (tokens == 0)
+        return AR_OK;
+    if (!src || !aligned16(src))
+        return fail(AR_ERR_INVALID, "src NULL or not 16-byte aligned");
+    mode = resolve_mode(ws, mode, tokens);
+    const uint64_t plane = (uint64_t)tokens * ws->H * 2;
+    const uint64_t nvec = plane / 16;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (mode == AR_MODE_LAMPORT) {
+        stage_kernel<<<grid_for(nvec, 256, ws->sms), 256, 0, s>>>(
+            static_cast<const uint4*>(src), ws->base + ws->lamport_off, ws->slot_bytes,
+            (uint64_t)rank * plane, nvec, 1, state_of(ws));
+    } else {
+        stage_kernel<<<grid_for(nvec, 256, ws->sms), 256, 0, s>>>(
+            static_cast<const uint4*>(src), ws->base + ws->buffer_off, 0,
+            (uint64_t)rank * ws->maxT * ws->H * 2, nvec, 0, state_of(ws));
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return cuda_fail(e, "stage kernel launch");
+    return AR_OK;
+}
+
+int ar_fusion_run(ar_fusion_ws* ws, const void* const* partials, int nranks, int tokens,
+                  int hidden_dim, int dtype, const void* residual_in, const void* gamma,
+                  float eps, int pattern, void* residual_out, void* norm_out, void* quant_out,
+                  void* scale_out, const float* scale_factor, void* stream)
+{
+    FusedArgs a;
+    bool launch = false;
+    int rc = prepare(ws, partials, nranks, tokens, hidden_dim, dtype, residual_in, gamma, eps,
+                     pattern, residual_out, norm_out, quant_out, scale_out, scale_factor, false, a,
+                     launch);
+    if (rc || !launch)
+        return rc;
+    return launch_fused(ws, a, static_cast<cudaStream_t>(stream));
+}
+
+int ar_fusion_norm_amax(ar_fusion_ws* ws, const void* const* partials, int nranks, int tokens,
+                        int hidden_dim, int dtype, const void* residual_in, const void* gamma,
+                        float eps, float* amax_out, void* stream)
+{
+    if (!amax_out || ((uintptr_t)amax_out & 3))
+        return fail(AR_ERR_INVALID, "amax_out NULL or misaligned");
+    FusedArgs a;
+    bool launch = false;
+    int rc = prepare(ws, partials, nranks, tokens, hidden_dim, dtype, residual_in, gamma, eps, 0,
+                     nullptr, nullptr, nullptr, nullptr, nullptr, true, a, launch);
+    if (rc)
+        return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float), s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaMemsetAsync(amax_out)");
+    if (!launch)
+        return AR_OK;
+    a.amax_out = amax_out;
+    const LaunchCfg c{ws->sms, s};
+    const int variant = a.H <= 1024 ? AR_VARIANT_WARP_ROW : AR_VARIANT_CTA_ROW;
+    e = launch_fused_rows(ws->dtype, variant, a, c);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "amax kernel launch");
+    return AR_OK;
+}
+
+int ar_fusion_sum(const void* const* bufs, int nranks, size_t n, int dtype, void* out,
+                  void* stream)
+{
+    if (dtype != AR_DT_BF16 && dtype != AR_DT_FP16)
+        return fail(AR_ERR_UNSUPPORTED, "dtype %d is not bf16 (0) or fp16 (1)", dtype);
+    if (nranks < 1 || nranks > AR_MAX_RANKS)
+        return fail(AR_ERR_UNSUPPORTED, "nranks %d outside 1..%d", nranks, AR_MAX_RANKS);
+    if (n == 0)
+        return AR_OK;
+    if (!bufs || !out || ((uintptr_t)out & 1))
+        return fail(AR_ERR_INVALID, "bufs / out NULL or out misaligned");
+    SumArgs a;
+    memset(&a, 0, sizeof a);
+    for (int r = 0; r < nranks; ++r) {
+        if (!bufs[r] || ((uintptr_t)bufs[r] & 1))
+            return fail(AR_ERR_INVALID, "bufs[%d] NULL or misaligned", r);
+        a.in[r] = static_cast<const uint8_t*>(bufs[r]);
+    }
+    a.out = static_cast<uint8_t*>(out);
+    a.R = nranks;
+    a.n = n;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "device query");
+    e = launch_vector_sum(dtype, a, LaunchCfg{sms, static_cast<cudaStream_t>(stream)});
+    if (e != cudaSuccess)
+        return cuda_fail(e, "sum kernel launch");
+    return AR_OK;
+}
+
+}  // extern "C"

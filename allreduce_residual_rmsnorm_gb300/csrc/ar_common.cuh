@@ -1,0 +1,249 @@
+// Device helpers shared by the sm_103a kernels of libarfusion.
+//
+// Element conversions use the hardware cvt instructions (round to nearest
+// even); no approximate math is used anywhere on the path: the RMSNorm
+// division and square root are the IEEE-rounded __fdiv_rn / __fsqrt_rn.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ar_fusion.h"
+
+namespace arf {
+
+struct Bf16 {
+    static constexpr int id = AR_DT_BF16;
+};
+struct Fp16 {
+    static constexpr int id = AR_DT_FP16;
+};
+
+// ------------------------------------------------------ 16-bit element pairs
+
+// Two elements packed in a 32-bit word (element 2i in the low half) -> fp32.
+// Both conversions are exact.
+template <class D>
+__device__ __forceinline__ float2 unpack2(uint32_t w);
+
+template <>
+__device__ __forceinline__ float2 unpack2<Bf16>(uint32_t w)
+{
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+template <>
+__device__ __forceinline__ float2 unpack2<Fp16>(uint32_t w)
+{
+    __half2 h;
+    memcpy(&h, &w, 4);
+    return __half22float2(h);
+}
+
+// fp32 pair -> packed pair, each rounded to nearest even.
+template <class D>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi);
+
+template <>
+__device__ __forceinline__ uint32_t pack2<Bf16>(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    uint32_t w;
+    memcpy(&w, &v, 4);
+    return w;
+}
+
+template <>
+__device__ __forceinline__ uint32_t pack2<Fp16>(float lo, float hi)
+{
+    __half2 v = __floats2half2_rn(lo, hi);
+    uint32_t w;
+    memcpy(&w, &v, 4);
+    return w;
+}
+
+// 8 elements of a 16-byte vector -> fp32
+template <class D>
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8])
+{
+    float2 p;
+    p = unpack2<D>(v.x); f[0] = p.x; f[1] = p.y;
+    p = unpack2<D>(v.y); f[2] = p.x; f[3] = p.y;
+    p = unpack2<D>(v.z); f[4] = p.x; f[5] = p.y;
+    p = unpack2<D>(v.w); f[6] = p.x; f[7] = p.y;
+}
+
+template <class D>
+__device__ __forceinline__ uint4 pack8(const float (&f)[8])
+{
+    uint4 v;
+    v.x = pack2<D>(f[0], f[1]);
+    v.y = pack2<D>(f[2], f[3]);
+    v.z = pack2<D>(f[4], f[5]);
+    v.w = pack2<D>(f[6], f[7]);
+    return v;
+}
+
+// ------------------------------------------------------------ memory ops
+
+// Streaming 128-bit load of data read exactly once (no L1 allocation).
+__device__ __forceinline__ uint4 ld_stream(const void* p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// 128-bit load that re-reads memory on every call (Lamport slot polling).
+__device__ __forceinline__ uint4 ld_poll(const void* p)
+{
+    uint4 v;
+    asm volatile("ld.volatile.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Cached 128-bit load (gamma: read by every row).
+__device__ __forceinline__ uint4 ld_keep(const void* p)
+{
+    return *reinterpret_cast<const uint4*>(p);
+}
+
+__device__ __forceinline__ void st_vec(void* p, const uint4& v)
+{
+    *reinterpret_cast<uint4*>(p) = v;
+}
+
+__device__ __forceinline__ void st_u2(void* p, uint32_t a, uint32_t b)
+{
+    *reinterpret_cast<uint2*>(p) = make_uint2(a, b);
+}
+
+// -0.0f sentinel test of TensorRT-LLM allReduceFusionKernels.cu (is_neg_zero):
+// a 32-bit word equal to 0x80000000 means "not yet written".
+__device__ __forceinline__ bool has_sentinel(const uint4& v)
+{
+    return (v.x == 0x80000000u) | (v.y == 0x80000000u) | (v.z == 0x80000000u) |
+           (v.w == 0x80000000u);
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void record_error(ar_fusion_state* st, int code, int detail)
+{
+    if (atomicCAS(&st->status, 0, code) == 0)
+        atomicExch(&st->detail, detail);
+}
+
+// ------------------------------------------------- double-float accumulation
+//
+// Sum of squares as an unevaluated pair (hi, lo): every square of a 16-bit
+// element is exact in fp32, and TwoSum keeps the rounding error of each
+// addition, so hi + lo carries ~48 significant bits.  The pair is rounded to
+// fp32 once at the end, which reproduces the correctly rounded sum except when
+// the exact sum sits within ~2^-44 (relative) of an fp32 rounding boundary.
+
+struct DF {
+    float hi, lo;
+};
+
+__device__ __forceinline__ void df_add_term(DF& a, float t)
+{
+    float s = __fadd_rn(a.hi, t);
+    float bb = __fadd_rn(s, -a.hi);
+    float err = __fadd_rn(__fadd_rn(a.hi, -__fadd_rn(s, -bb)), __fadd_rn(t, -bb));
+    a.hi = s;
+    a.lo = __fadd_rn(a.lo, err);
+}
+
+__device__ __forceinline__ DF df_add(DF a, DF b)
+{
+    float s = __fadd_rn(a.hi, b.hi);
+    float bb = __fadd_rn(s, -a.hi);
+    float err = __fadd_rn(__fadd_rn(a.hi, -__fadd_rn(s, -bb)), __fadd_rn(b.hi, -bb));
+    float lo = __fadd_rn(__fadd_rn(a.lo, b.lo), err);
+    float hi = __fadd_rn(s, lo);
+    lo = __fadd_rn(lo, -__fadd_rn(hi, s));
+    return DF{hi, lo};
+}
+
+__device__ __forceinline__ DF df_shfl_xor(DF a, int m)
+{
+    return DF{__shfl_xor_sync(0xffffffffu, a.hi, m), __shfl_xor_sync(0xffffffffu, a.lo, m)};
+}
+
+__device__ __forceinline__ DF df_warp_sum(DF a)
+{
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1)
+        a = df_add(a, df_shfl_xor(a, m));
+    return a;
+}
+
+// ----------------------------------------------------- FP8 / FP4 encoders
+//
+// PTX cvt with .satfinite: round to nearest even, finite overflow and
+// infinities saturate to the largest finite code, sign of zero kept.
+// Operand order: the first source lands in the upper part of the result.
+
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// 8 fp32 -> 8 E4M3 bytes (element 0 in the lowest byte)
+__device__ __forceinline__ uint2 e4m3x8(const float (&f)[8])
+{
+    uint2 o;
+    o.x = e4m3x2(f[0], f[1]) | (e4m3x2(f[2], f[3]) << 16);
+    o.y = e4m3x2(f[4], f[5]) | (e4m3x2(f[6], f[7]) << 16);
+    return o;
+}
+
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b8 q;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q, %1, %2;\n\t"
+        "cvt.u32.u8 %0, q;\n\t}"
+        : "=r"(r)
+        : "f"(hi), "f"(lo));
+    return r;
+}
+
+// 8 fp32 -> 8 E2M1 codes in 4 bytes (element 2k in the low nibble of byte k)
+__device__ __forceinline__ uint32_t e2m1x8(const float (&f)[8])
+{
+    return e2m1x2(f[0], f[1]) | (e2m1x2(f[2], f[3]) << 8) | (e2m1x2(f[4], f[5]) << 16) |
+           (e2m1x2(f[6], f[7]) << 24);
+}
+
+// E4M3 byte -> fp32 (exact: E4M3 values are a subset of fp16)
+__device__ __forceinline__ float e4m3_to_f32(uint32_t code)
+{
+    uint32_t h2;
+    uint16_t in = (uint16_t)code;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+    __half2 h;
+    memcpy(&h, &h2, 4);
+    return __low2float(h);
+}
+
+__device__ __forceinline__ uint32_t e4m3_byte(float v)
+{
+    return e4m3x2(v, 0.0f) & 0xffu;
+}
+
+}  // namespace arf

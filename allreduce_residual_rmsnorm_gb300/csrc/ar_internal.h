@@ -1,0 +1,51 @@
+// Host/device shared internals of libarfusion (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ar_fusion.h"
+
+namespace arf {
+
+// Everything one fused launch needs, passed by value as the kernel parameter.
+struct FusedArgs {
+    const uint8_t* partial[AR_MAX_RANKS];  // per-rank [T][H] bases (unused in Lamport mode)
+    int R, T, H, pattern;
+    const uint8_t* residual_in;
+    const uint8_t* gamma;
+    float eps;
+    uint8_t* residual_out;
+    uint8_t* norm_out;
+    uint8_t* quant_out;
+    uint8_t* scale_out;
+    const float* scale_factor;
+    float* amax_out;            // calibration pass: atomic max of |n| (as uint bits)
+    // Lamport (one-shot) staged mode
+    int lamport;
+    uint8_t* lamport_base;      // slot k at lamport_base + k * slot_bytes
+    uint64_t slot_bytes;
+    ar_fusion_state* state;     // status word always; slot state in Lamport mode
+    uint64_t timeout_ns;
+};
+
+struct LaunchCfg {
+    int sms;                    // multiprocessor count of the current device
+    cudaStream_t stream;
+};
+
+// Kernel launchers (return cudaError_t of the launch).  `variant` is a
+// concrete AR_VARIANT_* (never AUTO).
+cudaError_t launch_fused_rows(int dtype, int variant, const FusedArgs& a, const LaunchCfg& c);
+cudaError_t launch_fused_pipe(int dtype, const FusedArgs& a, const LaunchCfg& c);
+bool fused_pipe_supported(int dtype, int H, int R);
+
+struct SumArgs {
+    const uint8_t* in[AR_MAX_RANKS];
+    uint8_t* out;
+    int R;
+    uint64_t n;
+};
+cudaError_t launch_vector_sum(int dtype, const SumArgs& a, const LaunchCfg& c);
+
+}  // namespace arf

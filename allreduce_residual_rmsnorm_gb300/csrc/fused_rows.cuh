@@ -1,0 +1,289 @@
+// Register-resident fused epilogue: one row per warp or one row per block.
+//
+// Per token row (TensorRT-LLM allReduceFusionKernels.cu: allreduce_sum,
+// fused_op, add128, rms_norm):
+//   s = sum_r f(P_r)  (fp32, rank order)    a = rnd(s)
+//   y = rnd(f(a) + f(x))                    -> residual_out
+//   ss = sum y^2 (double-float pair, rounded once)
+//   rstd = 1 / sqrt(ss / H + eps)           (IEEE div / sqrt)
+//   n = rnd((y * rstd) * gamma)             -> norm_out, FP8 / NVFP4 codes
+//
+// Each row is split into 16-byte vectors of 8 elements; the thread with index
+// g in its group of G threads owns vectors v = g + k*G (k < VPT), so every
+// warp-wide load or store instruction covers 512 contiguous bytes.  The
+// summed row stays in registers between the sum of squares and the
+// normalisation: every input byte is read once.  An NVFP4 block (16
+// elements) is the vector pair (2j, 2j+1), held by neighbouring lanes, so the
+// block maximum takes one xor-1 shuffle.
+//
+// In Lamport mode the partials come from the current workspace slot and are
+// polled (bounded) until no 32-bit word holds the -0.0f sentinel; the
+// retired slot is refilled with the sentinel in the same launch and the last
+// block to finish advances the slot index (LamportComm::update without a
+// spin: an atomic ticket).
+#pragma once
+
+#include "ar_common.cuh"
+#include "ar_internal.h"
+
+namespace arf {
+
+template <class D, int RMAX, int VPT, bool WARP_ROW>
+__global__ void __launch_bounds__(WARP_ROW ? 256 : 512)
+fused_rows_kernel(const FusedArgs a)
+{
+    // vectors loaded per batch: keep about 16 x 16 B of partials in flight per thread
+    constexpr int KCH = (16 / RMAX) < 1 ? 1 : ((16 / RMAX) > VPT ? VPT : (16 / RMAX));
+    static_assert(VPT % KCH == 0, "batch must divide VPT");
+
+    const int H = a.H;
+    const int Hv = H >> 3;
+    const int R = a.R;
+    const int pat = a.pattern;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    int G, g, row, row_step;
+    if (WARP_ROW) {
+        G = 32;
+        g = lane;
+        row = blockIdx.x * nwarps + warp;
+        row_step = gridDim.x * nwarps;
+    } else {
+        G = blockDim.x;
+        g = threadIdx.x;
+        row = blockIdx.x;
+        row_step = gridDim.x;
+    }
+
+    const uint8_t* P[RMAX];
+    uint32_t flag = 0;
+    if (a.lamport) {
+        flag = *reinterpret_cast<volatile uint32_t*>(&a.state->lamport_flag);
+        const uint64_t clear_elems = *reinterpret_cast<volatile uint64_t*>(&a.state->clear_size);
+        const size_t plane = (size_t)a.T * H * 2;
+        const uint8_t* slot = a.lamport_base + (size_t)(flag % 3u) * a.slot_bytes;
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r)
+            P[r] = slot + (size_t)r * plane;
+        // refill the retired slot with the sentinel (clear loop of the one-shot kernel)
+        uint8_t* clr = a.lamport_base + (size_t)((flag + 2u) % 3u) * a.slot_bytes;
+        const uint64_t nvec = clear_elems / 8;
+        const uint64_t nth = (uint64_t)gridDim.x * blockDim.x;
+        const uint4 sent = make_uint4(0x80000000u, 0x80000000u, 0x80000000u, 0x80000000u);
+        for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += nth)
+            st_vec(clr + i * 16, sent);
+    } else {
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r)
+            P[r] = a.partial[r];
+    }
+
+    uint4 gv[VPT];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int v = g + k * G;
+        gv[k] = v < Hv ? ld_keep(a.gamma + (size_t)v * 16) : make_uint4(0, 0, 0, 0);
+    }
+    float qscale = 0.0f;
+    if (pat & (AR_QUANT_FP8 | AR_QUANT_NVFP4))
+        qscale = *a.scale_factor;
+
+    __shared__ DF red[2][32];
+    int parity = 0;
+    float amax_local = 0.0f;
+
+    for (; row < a.T; row += row_step) {
+        const size_t roff = (size_t)row * H * 2;
+        DF ss = {0.0f, 0.0f};
+        uint4 yv[VPT];
+
+#pragma unroll
+        for (int k0 = 0; k0 < VPT; k0 += KCH) {
+            uint4 raw[KCH][RMAX];
+            uint4 xr[KCH];
+            // ---- loads of this batch (all in flight together)
+#pragma unroll
+            for (int kk = 0; kk < KCH; ++kk) {
+                const int v = g + (k0 + kk) * G;
+                if (v < Hv) {
+#pragma unroll
+                    for (int r = 0; r < RMAX; ++r)
+                        if (r < R)
+                            raw[kk][r] = a.lamport ? ld_poll(P[r] + roff + (size_t)v * 16)
+                                                   : ld_stream(P[r] + roff + (size_t)v * 16);
+                    xr[kk] = ld_stream(a.residual_in + roff + (size_t)v * 16);
+                }
+            }
+            // ---- Lamport: re-poll until no sentinel word is left (bounded)
+            if (a.lamport) {
+                bool pend = false;
+#pragma unroll
+                for (int kk = 0; kk < KCH; ++kk)
+#pragma unroll
+                    for (int r = 0; r < RMAX; ++r)
+                        if (r < R && g + (k0 + kk) * G < Hv)
+                            pend |= has_sentinel(raw[kk][r]);
+                if (pend) {
+                    const uint64_t t0 = globaltimer_ns();
+                    while (true) {
+                        pend = false;
+                        int first = -1;
+#pragma unroll
+                        for (int kk = 0; kk < KCH; ++kk) {
+                            const int v = g + (k0 + kk) * G;
+#pragma unroll
+                            for (int r = 0; r < RMAX; ++r)
+                                if (r < R && v < Hv && has_sentinel(raw[kk][r])) {
+                                    raw[kk][r] = ld_poll(P[r] + roff + (size_t)v * 16);
+                                    if (has_sentinel(raw[kk][r])) {
+                                        pend = true;
+                                        if (first < 0)
+                                            first = r;
+                                    }
+                                }
+                        }
+                        if (!pend)
+                            break;
+                        if (globaltimer_ns() - t0 > a.timeout_ns) {
+                            record_error(a.state, AR_ERR_TIMEOUT, row * 32 + first);
+                            break;
+                        }
+                        __nanosleep(256);
+                    }
+                }
+            }
+            // ---- rank sum, residual add, sum of squares
+#pragma unroll
+            for (int kk = 0; kk < KCH; ++kk) {
+                const int k = k0 + kk;
+                const int v = g + k * G;
+                if (v < Hv) {
+                    float s[8];
+                    unpack8<D>(raw[kk][0], s);
+#pragma unroll
+                    for (int r = 1; r < RMAX; ++r) {
+                        if (r < R) {
+                            float t[8];
+                            unpack8<D>(raw[kk][r], t);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                s[i] = __fadd_rn(s[i], t[i]);
+                        }
+                    }
+                    float af[8], xf[8];
+                    unpack8<D>(pack8<D>(s), af);
+                    unpack8<D>(xr[kk], xf);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        af[i] = __fadd_rn(af[i], xf[i]);
+                    const uint4 y = pack8<D>(af);
+                    yv[k] = y;
+                    if (pat & AR_RESIDUAL_OUT)
+                        st_vec(a.residual_out + roff + (size_t)v * 16, y);
+                    float yf[8];
+                    unpack8<D>(y, yf);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        df_add_term(ss, __fmul_rn(yf[i], yf[i]));
+                } else {
+                    yv[k] = make_uint4(0, 0, 0, 0);
+                }
+            }
+        }
+
+        // ---- sum of squares over the row
+        ss = df_warp_sum(ss);
+        if (!WARP_ROW) {
+            if (lane == 0)
+                red[parity][warp] = ss;
+            __syncthreads();
+            DF tot = red[parity][0];
+            for (int w = 1; w < nwarps; ++w)
+                tot = df_add(tot, red[parity][w]);
+            ss = tot;
+            parity ^= 1;
+        }
+        const float ss32 = __fadd_rn(ss.hi, ss.lo);
+        const float ms = __fdiv_rn(ss32, (float)H);
+        const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, a.eps)));
+
+        // ---- normalise, optional outputs
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int v = g + k * G;
+            const bool ok = v < Hv;
+            float yf[8], gf[8], nf[8];
+            unpack8<D>(yv[k], yf);
+            unpack8<D>(gv[k], gf);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                nf[i] = __fmul_rn(__fmul_rn(yf[i], rstd), gf[i]);
+            const uint4 nv = pack8<D>(nf);
+            if (ok && (pat & AR_NORM_OUT))
+                st_vec(a.norm_out + roff + (size_t)v * 16, nv);
+            float nq[8];
+            unpack8<D>(nv, nq);
+            if (a.amax_out && ok) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    amax_local = fmaxf(amax_local, fabsf(nq[i]));
+            }
+            if (pat & AR_QUANT_FP8) {
+                float t[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    t[i] = __fmul_rn(nq[i], qscale);
+                const uint2 c = e4m3x8(t);
+                if (ok)
+                    st_u2(a.quant_out + (size_t)row * H + (size_t)v * 8, c.x, c.y);
+            }
+            if (pat & AR_QUANT_NVFP4) {
+                float bm = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    bm = fmaxf(bm, fabsf(nq[i]));
+                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+                const uint32_t sf = e4m3_byte(__fmul_rn(qscale, __fdiv_rn(bm, 6.0f)));
+                const float dec = e4m3_to_f32(sf);
+                const float enc = dec == 0.0f ? 0.0f : __fdiv_rn(qscale, dec);
+                float t[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    t[i] = __fmul_rn(nq[i], enc);
+                const uint32_t codes = e2m1x8(t);
+                if (ok) {
+                    *reinterpret_cast<uint32_t*>(a.quant_out + (size_t)row * (H / 2) +
+                                                 (size_t)v * 4) = codes;
+                    if ((v & 1) == 0)
+                        a.scale_out[(size_t)row * (H / 16) + (v >> 1)] = (uint8_t)sf;
+                }
+            }
+        }
+    }
+
+    if (a.amax_out) {
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1)
+            amax_local = fmaxf(amax_local, __shfl_xor_sync(0xffffffffu, amax_local, m));
+        if (lane == 0)
+            atomicMax(reinterpret_cast<unsigned int*>(a.amax_out), __float_as_uint(amax_local));
+    }
+
+    if (a.lamport) {
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            const unsigned prev = atomicAdd(&a.state->counter, 1u);
+            if (prev == gridDim.x - 1) {
+                a.state->lamport_flag = (flag + 1u) % 3u;
+                a.state->clear_size = (uint64_t)R * a.T * H;
+                a.state->calls += 1;
+                a.state->counter = 0;
+                __threadfence();
+            }
+        }
+    }
+}
+
+}  // namespace arf

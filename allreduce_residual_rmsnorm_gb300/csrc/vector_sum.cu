@@ -1,0 +1,160 @@
+// Plain R-way sum, out[i] = rnd(sum_r f(in_r[i])) in fp32, rank order
+// (mscclpp allreduce.cu: vectorSum, here out of place over R inputs and with
+// fp32 accumulation).
+//
+// 16-byte aligned inputs: grid-stride over 16-byte vectors, two vectors per
+// thread per step so 2R loads are in flight, and the n % 8 tail elements done
+// one by one (the page's vectorSum drops nothing either: its 32-bit tail loop
+// covers the rest).  Any misaligned pointer: element-wise kernel.
+#include "ar_common.cuh"
+#include "ar_internal.h"
+
+namespace arf {
+
+template <class D>
+__device__ __forceinline__ float ld_elem(const uint8_t* p, uint64_t i)
+{
+    const uint16_t b = reinterpret_cast<const uint16_t*>(p)[i];
+    if constexpr (D::id == AR_DT_BF16) {
+        return __uint_as_float((uint32_t)b << 16);
+    } else {
+        __half h;
+        memcpy(&h, &b, 2);
+        return __half2float(h);
+    }
+}
+
+template <class D>
+__device__ __forceinline__ void st_elem(uint8_t* p, uint64_t i, float v)
+{
+    uint16_t b;
+    if constexpr (D::id == AR_DT_BF16) {
+        __nv_bfloat16 h = __float2bfloat16_rn(v);
+        memcpy(&b, &h, 2);
+    } else {
+        __half h = __float2half_rn(v);
+        memcpy(&b, &h, 2);
+    }
+    reinterpret_cast<uint16_t*>(p)[i] = b;
+}
+
+template <class D, int RMAX>
+__device__ __forceinline__ uint4 sum_vec(const SumArgs& a, const uint4 (&raw)[RMAX])
+{
+    float s[8];
+    unpack8<D>(raw[0], s);
+#pragma unroll
+    for (int r = 1; r < RMAX; ++r) {
+        if (r < a.R) {
+            float t[8];
+            unpack8<D>(raw[r], t);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                s[i] = __fadd_rn(s[i], t[i]);
+        }
+    }
+    return pack8<D>(s);
+}
+
+template <class D, int RMAX>
+__global__ void __launch_bounds__(256) vector_sum_kernel(const SumArgs a)
+{
+    const uint64_t nvec = a.n / 8;
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    uint64_t i = tid;
+    for (; i + stride < nvec; i += 2 * stride) {
+        uint4 r0[RMAX], r1[RMAX];
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r) {
+            if (r < a.R) {
+                r0[r] = ld_stream(a.in[r] + i * 16);
+                r1[r] = ld_stream(a.in[r] + (i + stride) * 16);
+            }
+        }
+        st_vec(a.out + i * 16, sum_vec<D, RMAX>(a, r0));
+        st_vec(a.out + (i + stride) * 16, sum_vec<D, RMAX>(a, r1));
+    }
+    if (i < nvec) {
+        uint4 r0[RMAX];
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r)
+            if (r < a.R)
+                r0[r] = ld_stream(a.in[r] + i * 16);
+        st_vec(a.out + i * 16, sum_vec<D, RMAX>(a, r0));
+    }
+    const uint64_t tail = a.n - nvec * 8;
+    if (tid < tail) {
+        const uint64_t e = nvec * 8 + tid;
+        float s = ld_elem<D>(a.in[0], e);
+        for (int r = 1; r < a.R; ++r)
+            s = __fadd_rn(s, ld_elem<D>(a.in[r], e));
+        st_elem<D>(a.out, e, s);
+    }
+}
+
+template <class D>
+__global__ void __launch_bounds__(256) vector_sum_scalar_kernel(const SumArgs a)
+{
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    for (uint64_t e = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; e < a.n; e += stride) {
+        float s = ld_elem<D>(a.in[0], e);
+        for (int r = 1; r < a.R; ++r)
+            s = __fadd_rn(s, ld_elem<D>(a.in[r], e));
+        st_elem<D>(a.out, e, s);
+    }
+}
+
+template <class D>
+static const void* sum_fn(int rmax)
+{
+    switch (rmax) {
+    case 2: return (const void*)vector_sum_kernel<D, 2>;
+    case 4: return (const void*)vector_sum_kernel<D, 4>;
+    case 8: return (const void*)vector_sum_kernel<D, 8>;
+    case 16: return (const void*)vector_sum_kernel<D, 16>;
+    default: return nullptr;
+    }
+}
+
+template <class D>
+static cudaError_t launch_t(const SumArgs& a, const LaunchCfg& c)
+{
+    bool aligned = ((uintptr_t)a.out & 15) == 0;
+    for (int r = 0; r < a.R; ++r)
+        aligned = aligned && ((uintptr_t)a.in[r] & 15) == 0;
+    const int threads = 256;
+    void* args[] = {const_cast<SumArgs*>(&a)};
+    if (!aligned) {
+        uint64_t blocks = (a.n + threads - 1) / threads;
+        const uint64_t cap = (uint64_t)c.sms * 8;
+        if (blocks > cap)
+            blocks = cap;
+        if (blocks < 1)
+            blocks = 1;
+        return cudaLaunchKernel((const void*)vector_sum_scalar_kernel<D>, dim3((unsigned)blocks),
+                                dim3(threads), args, 0, c.stream);
+    }
+    const int rmax = a.R <= 2 ? 2 : a.R <= 4 ? 4 : a.R <= 8 ? 8 : 16;
+    const void* fn = sum_fn<D>(rmax);
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, 0) != cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    const uint64_t nvec = a.n / 8;
+    // two vectors per thread per step; at least one block (the tail needs it)
+    uint64_t blocks = (nvec + 2 * threads - 1) / (2 * threads);
+    const uint64_t cap = (uint64_t)c.sms * per_sm;
+    if (blocks > cap)
+        blocks = cap;
+    if (blocks < 1)
+        blocks = 1;
+    return cudaLaunchKernel(fn, dim3((unsigned)blocks), dim3(threads), args, 0, c.stream);
+}
+
+cudaError_t launch_vector_sum(int dtype, const SumArgs& a, const LaunchCfg& c)
+{
+    return dtype == AR_DT_BF16 ? launch_t<Bf16>(a, c) : launch_t<Fp16>(a, c);
+}
+
+}  // namespace arf

@@ -13,7 +13,7 @@ Recipe (one CPU ``torch.Generator`` seeded with ``seed``, draws in this order):
       partial_r = base_r rounded (RNE) to D
   residual = randn(T, H) * x_std  -> D
   gamma    = 1 + randn(H) * g_std  -> D
-Plain R-way sum inputs: (rand(R, N) * 2 - 1) -> D, i.e. U(-1, 1).
+Plain R-way sum inputs: for each rank, (rand(N) * 2 - 1) -> D, i.e. U(-1, 1).
 """
 from __future__ import annotations
 
@@ -115,7 +115,10 @@ def make_sum_inputs(w: SumWorkload) -> torch.Tensor:
     g = torch.Generator(device="cpu")
     g.manual_seed(w.seed)
     dt = torch_dtype(w.dtype)
-    return (torch.rand((w.R, w.N), generator=g, dtype=torch.float32) * 2.0 - 1.0).to(dt)
+    out = torch.empty((w.R, w.N), dtype=dt)
+    for r in range(w.R):
+        out[r].copy_(torch.rand((w.N,), generator=g, dtype=torch.float32).mul_(2.0).sub_(1.0))
+    return out
 
 
 def bits(t: torch.Tensor):

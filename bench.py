@@ -1,0 +1,406 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused allreduce epilogue on GB300.
+
+Workload: R=8 rank partials, T=8192 tokens, H=7168, bf16, residual_out +
+NVFP4 (16-element blocks, E4M3 block scales, fp32 global scale); partials
+staged in the workspace buffer region.  One step = one ar_fusion_run.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line (rank 0).  Under torchrun with N > 1 every rank runs an
+independent replica of the workload on its own GPU (nothing is exchanged
+between GPUs); value = tokens processed by all ranks / max-over-ranks time.
+``--impl reference`` times the CPU oracle on the host cores on bounded samples
+of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused AR+RMSNorm tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+KERNEL_SOURCES = ["ar_common.cuh", "fused_pipe.cu", "fused_rows.cuh", "fused_rows_impl.cuh",
+                  "ar_api.cu"]
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--e2e-steps", type=int, default=None)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--variant", default="auto", choices=["auto", "cta", "pipe", "warp"])
+    return p.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def algorithmic_bytes(R, T, H, elem=2):
+    # partials + residual_in + residual_out + NVFP4 codes + E4M3 block scales
+    return R * T * H * elem + 2 * T * H * elem + T * H // 2 + T * H // 16
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "allreduce_residual_rmsnorm_gb300", "csrc")
+    for f in sorted(KERNEL_SOURCES):
+        p = os.path.join(csrc, f)
+        if os.path.exists(p):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_name):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic_r8_t8192_h7168_nvfp4.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for ln in open(path):
+        if ":" in ln and not ln.startswith("#"):
+            k, v = ln.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("kernel_sources_sha256_16") != kernel_hash():
+        return None
+    if kernel_name and vals.get("kernel") and kernel_name not in vals.get("kernel"):
+        return None
+    try:
+        return int(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while running."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "25"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append((time.time(), ln.strip()))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 10:
+                continue
+            rows.append((ts, f))
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        win = [f for ts, f in rows if t0 - 0.05 <= ts <= t1 + 0.05] or [rows[-1][1]]
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(f[2]) for f in win if num(f[2]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for f in win:
+            for n, v in zip(names, f[6:10]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(win[0][3]), "reasons": sorted(reasons), "samples": len(win),
+                "power_w_max": max((num(f[4]) or 0.0) for f in win)}
+
+
+def cpu_oracle_sample(w, inp, target_s=12.0, min_rows=16):
+    """Times the CPU oracle (fused rows + amax + NVFP4) over a bounded row
+    sample; returns (tokens/s, rows, seconds, threads)."""
+    import oracle
+    P = inp["P_bits"]
+    X = inp["X_bits"]
+    G = inp["G_bits"]
+    threads = oracle.host_threads()
+
+    def run(rows):
+        t0 = time.perf_counter()
+        sub_p = P[:, :rows]
+        res, nrm, _ = oracle.fused(oracle.BF16, sub_p, X[:rows], G, w.eps, threads=threads)
+        amax = oracle.amax(oracle.BF16, nrm)
+        oracle.quant_nvfp4(oracle.BF16, nrm, oracle.nvfp4_global_scale(amax))
+        return time.perf_counter() - t0
+
+    rows = min_rows
+    dt = run(rows)
+    rows = int(min(w.T, max(min_rows, rows * target_s / max(dt, 1e-6))))
+    dt = run(rows)
+    return rows / dt, rows, dt, threads
+
+
+def make_inputs(w):
+    from allreduce_residual_rmsnorm_gb300 import workloads as W
+    inp = W.make_fused_inputs(w)
+    return {"P": inp.partials, "X": inp.residual, "G": inp.gamma,
+            "P_bits": W.bits(inp.partials), "X_bits": W.bits(inp.residual),
+            "G_bits": W.bits(inp.gamma)}
+
+
+def run_reference(args, w):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    inp = make_inputs(w)
+    per_step = []
+    import oracle
+    oracle.build_oracle()
+    for i in range(args.warmup + args.steps):
+        tps, rows, dt, threads = cpu_oracle_sample(w, inp, target_s=2.0)
+        if i >= args.warmup:
+            per_step.append((tps, rows, dt))
+    tps = statistics.median(t for t, _, _ in per_step)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.median(d for _, _, d in per_step),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": config_of(w, "cpu oracle"),
+        "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"rows 0..{per_step[-1][1]} of {w.T} per step "
+                                   "(fused rows + amax + NVFP4, C oracle, row-parallel)"},
+        "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w, variant):
+    return {"workload": f"{w.name}: R={w.R} ranks, T={w.T} tokens, H={w.H}, bf16, "
+                        "residual_out + NVFP4 (16-elem blocks, E4M3 scales), partials staged in "
+                        "the workspace buffer region",
+            "R": w.R, "T": w.T, "H": w.H, "pattern": "residual_out|nvfp4", "variant": variant,
+            "l2": "inputs 1.21 GB > 129 MB L2 (no flush needed)", "parallelism": "replicas"}
+
+
+def main():
+    args = parse()
+    from allreduce_residual_rmsnorm_gb300 import workloads as W
+    w = W.NVFP4_PREFILL
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    import torch
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    import __graft_entry__
+    __graft_entry__.build() if rank == 0 or world == 1 else None
+    if pg:
+        pg.barrier()
+    from allreduce_residual_rmsnorm_gb300 import binding as B
+    B.load()
+
+    inp = make_inputs(w)
+    R, T, H = w.R, w.T, w.H
+    stream = torch.cuda.current_stream(dev)
+    ws = B.ar_fusion_workspace_create(R, T, H, B.AR_DT_BF16)
+    variant = {"auto": B.AR_VARIANT_AUTO, "cta": B.AR_VARIANT_CTA_ROW,
+               "pipe": B.AR_VARIANT_BULK_PIPE, "warp": B.AR_VARIANT_WARP_ROW}[args.variant]
+    B.ar_fusion_workspace_set_variant(ws, variant)
+    P = inp["P"].to(dev)
+    X = inp["X"].to(dev)
+    G = inp["G"].to(dev)
+    for r in range(R):
+        B.ar_fusion_workspace_stage(ws, r, P[r], mode=B.AR_MODE_BUFFER)
+    res = torch.empty_like(X)
+    q = torch.empty(T, H // 2, dtype=torch.uint8, device=dev)
+    sf = torch.empty(T, H // 16, dtype=torch.uint8, device=dev)
+    # per-tensor global scale from the library's own calibration pass (untimed)
+    amax = torch.empty(1, dtype=torch.float32, device=dev)
+    B.ar_fusion_norm_amax(ws, None, X, G, w.eps, amax)
+    torch.cuda.synchronize(dev)
+    gs = torch.tensor([2688.0 / float(amax.item())], dtype=torch.float32, device=dev)
+    pattern = B.PATTERNS[w.pattern]
+
+    def step():
+        B.ar_fusion_run(ws, None, X, G, w.eps, pattern, residual_out=res, quant_out=q,
+                        scale_out=sf, scale_factor=gs, stream=stream)
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    t_host0 = time.time()
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    g1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_host1 = time.time()
+    if pg:
+        pg.barrier()
+    total_ms = g0.elapsed_time(g1)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    avg_launch_s = sum(launch_ms) / len(launch_ms) / 1e3
+    time.sleep(0.1)
+    clocks.stop()
+    clk = clocks.summary(t_host0, t_host1)
+
+    if pg:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # ---- end to end: pinned host inputs -> device, run, outputs -> host
+    e2e_steps = args.e2e_steps or max(3, min(args.steps, 10))
+    Ph = inp["P"].pin_memory()
+    Xh = inp["X"].pin_memory()
+    Pd = torch.empty_like(P)
+    Xd = torch.empty_like(X)
+    res_h = torch.empty(res.shape, dtype=res.dtype).pin_memory()
+    q_h = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    sf_h = torch.empty(sf.shape, dtype=sf.dtype).pin_memory()
+
+    def e2e_step():
+        Pd.copy_(Ph, non_blocking=True)
+        Xd.copy_(Xh, non_blocking=True)
+        B.ar_fusion_run(ws, [Pd[r] for r in range(R)], Xd, G, w.eps, pattern, residual_out=res,
+                        quant_out=q, scale_out=sf, scale_factor=gs, stream=stream)
+        res_h.copy_(res, non_blocking=True)
+        q_h.copy_(q, non_blocking=True)
+        sf_h.copy_(sf, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+    if pg:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = Ph.numel() * Ph.element_size() + Xh.numel() * Xh.element_size()
+    d2h = (res_h.numel() * res_h.element_size() + q_h.numel() + sf_h.numel())
+
+    rc, detail = B.ar_fusion_workspace_status(ws)
+    if rc != 0:
+        raise SystemExit(f"device status {rc} (detail {detail})")
+
+    if rank != 0:
+        B.ar_fusion_workspace_destroy(ws)
+        if pg:
+            pg.destroy_process_group()
+        return
+
+    bytes_alg = algorithmic_bytes(R, T, H)
+    peak, peak_kind = measured_peak()
+    achieved = bytes_alg / avg_launch_s / 1e9
+    last = B.ar_fusion_workspace_info(ws)["last_variant"]
+    used_variant = {B.AR_VARIANT_CTA_ROW: "cta_row", B.AR_VARIANT_BULK_PIPE: "bulk_pipe",
+                    B.AR_VARIANT_WARP_ROW: "warp_row"}.get(last, "none")
+    kname = "fused_pipe_kernel" if last == B.AR_VARIANT_BULK_PIPE else "fused_rows_kernel"
+    line = {
+        "metric": METRIC,
+        "value": world * T * args.steps / (total_ms / 1e3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": config_of(w, used_variant),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": profiled_traffic(kname),
+                     "peak_kind": f"{peak_kind} (hbm_gbs, copy bandwidth)",
+                     "algorithmic_bytes_per_launch": bytes_alg,
+                     "avg_launch_us": avg_launch_s * 1e6},
+        "e2e": {"value": world * T * e2e_steps / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        tps, rows, dt, threads = cpu_oracle_sample(w, inp)
+        line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                                "sample": f"rows 0..{rows} of {w.T} ({dt:.1f} s): fused rows + amax "
+                                          "+ NVFP4, C oracle, row-parallel threads"}
+    print(json.dumps(line), flush=True)
+    B.ar_fusion_workspace_destroy(ws)
+    if pg:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,301 @@
+/*
+ * ar_fusion.h -- C ABI of the GB300 allreduce-fusion epilogue library
+ * (libarfusion.so, sm_103a).
+ *
+ * The operation (per token row t of a [tokens][hidden] problem, element type D
+ * = bf16 or fp16):
+ *
+ *   s_h  = P_0[t][h] + P_1[t][h] + ... + P_{R-1}[t][h]  (fp32, rank order)
+ *   a_h  = round_D(s_h)
+ *   y_h  = round_D(a_h + residual_in[t][h])                -> residual_out
+ *   rstd = 1 / sqrt(sum_h y_h^2 / hidden + eps)            (fp32)
+ *   n_h  = round_D((y_h * rstd) * gamma_h)                 -> norm_out
+ *   optional: FP8 E4M3 per-tensor codes of n, or NVFP4 codes + E4M3 block
+ *   scales of n                                            -> quant_out, scale_out
+ *
+ * Sources (page title, function):
+ *   TensorRT-LLM cpp/tensorrt_llm/kernels/allReduceFusionKernels.cu --
+ *     allreduce_sum (fp32 accumulation in rank order, Fp32Acc), add128 and
+ *     fused_op (residual add, optional outputs), rms_norm (sum of squares,
+ *     acc / hidden_dim + eps, x * s * gamma), allreduce_fusion_op (argument
+ *     checks and the four output patterns), LamportComm and
+ *     allreduce_fusion_kernel_oneshot_lamport (triple-buffered slots, -0.0
+ *     sentinel, retired-slot clear), lamport_initialize, Workspace.
+ *   FlashInfer docs, flashinfer.comm.trtllm_create_ipc_workspace_for_all_reduce_fusion
+ *     (workspace regions [buffer, flags, lamport x3], metadata fields).
+ *   mscclpp python/mscclpp_benchmark/allreduce.cu -- vectorSum (plain R-way sum).
+ *
+ * One GPU.  The R rank partials that a tensor-parallel all-reduce would
+ * exchange are R device buffers: either caller-owned pointers, or regions of
+ * the workspace filled with ar_fusion_workspace_stage().  Nothing crosses
+ * GPUs.
+ *
+ * Conventions for every entry point:
+ *   - Device pointers are plain CUDA device addresses; `stream` is a
+ *     cudaStream_t passed as void* (NULL = legacy default stream).
+ *   - All calls that launch work are asynchronous on `stream` and never
+ *     synchronise the device.  Exceptions, stated per call: create, destroy,
+ *     status and copy_state synchronise `stream`.
+ *   - Every call returns an ar_status code and never throws or aborts.  Invalid
+ *     arguments are rejected before anything is launched.  The message for the
+ *     last failure on the calling thread is ar_fusion_last_error().
+ *   - All device pointers must be 16-byte aligned (AR_ERR_INVALID otherwise).
+ *   - The caller owns every tensor; the library owns the workspace object and,
+ *     unless the caller supplied it, the workspace memory.
+ *   - Device-side waits are bounded: a wait that gives up records
+ *     AR_ERR_TIMEOUT in the workspace status word (ar_fusion_workspace_status)
+ *     instead of hanging the GPU.
+ */
+#ifndef AR_FUSION_H
+#define AR_FUSION_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------ constants -- */
+
+/* Element types of partials, residual, gamma and the 16-bit outputs. */
+enum ar_dtype {
+    AR_DT_BF16 = 0,
+    AR_DT_FP16 = 1
+};
+
+/* Output pattern bits.  Valid patterns are the four of allreduce_fusion_op
+ * (TensorRT-LLM allReduceFusionKernels.cu), with QUANT = exactly one of
+ * AR_QUANT_FP8 / AR_QUANT_NVFP4:
+ *     RESIDUAL_OUT | QUANT            NORM_OUT
+ *     RESIDUAL_OUT | NORM_OUT         RESIDUAL_OUT | NORM_OUT | QUANT      */
+enum ar_pattern {
+    AR_RESIDUAL_OUT = 1,
+    AR_NORM_OUT = 2,
+    AR_QUANT_FP8 = 4,
+    AR_QUANT_NVFP4 = 8
+};
+
+enum ar_status {
+    AR_OK = 0,
+    AR_ERR_INVALID = -1,      /* bad argument (null, misaligned, bad pattern ...) */
+    AR_ERR_UNSUPPORTED = -2,  /* valid request outside what the kernels implement */
+    AR_ERR_CUDA = -3,         /* a CUDA runtime call failed; see ar_fusion_last_error */
+    AR_ERR_TIMEOUT = -4,      /* a bounded device-side wait gave up */
+    AR_ERR_CAPACITY = -5      /* tokens > max_token_num of the workspace */
+};
+
+/* Where ar_fusion_run reads the partials from when `partials` is NULL. */
+enum ar_mode {
+    AR_MODE_AUTO = 0,         /* tokens <= AR_ONESHOT_MAX_TOKENS -> LAMPORT, else BUFFER */
+    AR_MODE_LAMPORT = 1,      /* current Lamport slot: polled for the -0.0 sentinel,
+                                 retired slot cleared, slot index advanced */
+    AR_MODE_BUFFER = 2        /* the buffer region, rank r at r * max_token_num * hidden */
+};
+
+/* Kernel variant (normally chosen by hidden size and token count). */
+enum ar_variant {
+    AR_VARIANT_AUTO = 0,
+    AR_VARIANT_WARP_ROW = 1,  /* one row per warp (small hidden) */
+    AR_VARIANT_CTA_ROW = 2,   /* one row per thread block, loads straight to registers */
+    AR_VARIANT_BULK_PIPE = 3  /* persistent blocks, rank rows streamed into shared
+                                 memory by bulk async copies (large token counts) */
+};
+
+#define AR_MAX_RANKS 16
+/* Token count up to which AR_MODE_AUTO uses the Lamport (one-shot) slots. The
+ * page's kOneShotMaxToken lives in a header that is not on the pages; this
+ * value is ours. */
+#define AR_ONESHOT_MAX_TOKENS 128
+/* Barrier flag words per rank in the flags region (the page's
+ * kBarrierFlagCount is not on the pages; ours).  Reserved: one GPU needs no
+ * cross-rank barrier. */
+#define AR_BARRIER_FLAG_COUNT 256
+#define AR_MAX_HIDDEN 32768
+
+typedef struct ar_fusion_ws ar_fusion_ws;   /* opaque, library-owned */
+
+/* Workspace description (FlashInfer workspace metadata fields, plus device
+ * addresses of each region).  Byte sizes are 64-bit: the page's `int` sizes
+ * overflow at 8 ranks x 8192 tokens x 7168 hidden. */
+typedef struct ar_fusion_ws_info {
+    int32_t tp_size;               /* R */
+    int32_t max_token_num;
+    int32_t hidden_dim;
+    int32_t dtype;                 /* enum ar_dtype */
+    int32_t elem_bytes;            /* 2 */
+    int32_t oneshot_max_tokens;    /* AR_ONESHOT_MAX_TOKENS */
+    uint64_t total_bytes;          /* whole workspace */
+    uint64_t buffer_bytes;         /* R * max_token_num * hidden * elem */
+    uint64_t flag_bytes;           /* R * AR_BARRIER_FLAG_COUNT * 4 */
+    uint64_t lamport_comm_bytes;   /* one slot: R * max(oneshot, max_token_num) * hidden * elem */
+    uint64_t lamport_buffer_bytes; /* three slots */
+    uint64_t state_bytes;          /* the state block (struct ar_fusion_state) */
+    void* base;                    /* device address of the workspace */
+    void* buffer;                  /* base + 0 */
+    void* flags;
+    void* lamport;                 /* slot k at lamport + k * lamport_comm_bytes */
+    void* state;                   /* struct ar_fusion_state */
+    int32_t last_variant;          /* enum ar_variant the last fused launch used (0: none yet) */
+    int32_t pad0;
+} ar_fusion_ws_info;
+
+/* Device-resident state (the page's 5-int flag array, widened).  Read it with
+ * ar_fusion_workspace_copy_state.  Order of the first fields follows the page:
+ * counter, flag, lamport flag, lamport comm size, clear size. */
+typedef struct ar_fusion_state {
+    uint32_t counter;        /* blocks finished in the current launch (0 between calls) */
+    uint32_t flag;           /* reserved (non-Lamport flag; unused on one GPU) */
+    uint32_t lamport_flag;   /* current slot = lamport_flag % 3 */
+    uint32_t pad0;
+    uint64_t comm_size;      /* bytes of one Lamport slot */
+    uint64_t clear_size;     /* elements of the retired slot still to be cleared */
+    int32_t status;          /* AR_OK or the first device-side error (AR_ERR_TIMEOUT) */
+    int32_t detail;          /* where it happened: row * 32 + rank, or -1 */
+    uint64_t calls;          /* Lamport-mode calls since create / reset */
+} ar_fusion_state;
+
+/* ------------------------------------------------------------ workspace -- */
+
+/* Bytes of device memory a workspace needs (for caller-supplied memory).
+ * Regions, in order and each 256-byte aligned: buffer, flags, three Lamport
+ * slots, state.  Returns AR_OK or AR_ERR_INVALID / AR_ERR_UNSUPPORTED. */
+int ar_fusion_workspace_bytes(int tp_size, int max_token_num, int hidden_dim, int dtype,
+                              size_t* bytes);
+
+/* Create a workspace (Workspace constructor of TensorRT-LLM
+ * allReduceFusionKernels.cu; FlashInfer trtllm_create_ipc_workspace_for_all_reduce_fusion).
+ *   tp_size        R, 1..AR_MAX_RANKS
+ *   max_token_num  largest `tokens` any later call may pass, >= 1
+ *   hidden_dim     row length, multiple of 8, <= AR_MAX_HIDDEN
+ *   dtype          enum ar_dtype
+ *   device_mem     NULL: the library allocates (cudaMalloc) and frees the memory.
+ *                  Otherwise caller-owned device memory of at least
+ *                  ar_fusion_workspace_bytes() bytes, 256-byte aligned, which
+ *                  must outlive the workspace.
+ *   stream         stream for the initialisation kernels (the Lamport region
+ *                  is filled with -0.0f words, lamport_initialize; the rest is
+ *                  zeroed); this call synchronises it.
+ *   out            receives the handle.
+ * Errors: AR_ERR_INVALID, AR_ERR_UNSUPPORTED, AR_ERR_CUDA (allocation). */
+int ar_fusion_workspace_create(int tp_size, int max_token_num, int hidden_dim, int dtype,
+                               void* device_mem, size_t device_mem_bytes, void* stream,
+                               ar_fusion_ws** out);
+
+/* Synchronise the device, free library-owned memory, free the handle.
+ * NULL is accepted (no-op). */
+int ar_fusion_workspace_destroy(ar_fusion_ws* ws);
+
+/* Fill *info.  No CUDA call. */
+int ar_fusion_workspace_info(const ar_fusion_ws* ws, ar_fusion_ws_info* info);
+
+/* Copy the device state block to host memory *out (synchronises `stream`). */
+int ar_fusion_workspace_copy_state(ar_fusion_ws* ws, void* stream, ar_fusion_state* out);
+
+/* Synchronise `stream`, read the device status word: returns AR_OK, the
+ * recorded device error (AR_ERR_TIMEOUT), or AR_ERR_CUDA.  *detail (may be
+ * NULL) receives row * 32 + rank of the first failed wait, or -1. */
+int ar_fusion_workspace_status(ar_fusion_ws* ws, void* stream, int* detail);
+
+/* Re-initialise on `stream`: Lamport region back to -0.0f words, slot index
+ * and clear size to 0, status to AR_OK.  Asynchronous. */
+int ar_fusion_workspace_reset(ar_fusion_ws* ws, void* stream);
+
+/* Bound, in nanoseconds, of each device-side wait of later launches
+ * (default 2e9).  Host-side setting; no CUDA call. */
+int ar_fusion_workspace_set_timeout_ns(ar_fusion_ws* ws, uint64_t ns);
+
+/* Force a kernel variant (enum ar_variant) or staged-read mode (enum
+ * ar_mode) for later calls on this workspace; AUTO restores the default
+ * choice.  Host-side settings; no CUDA call. */
+int ar_fusion_workspace_set_variant(ar_fusion_ws* ws, int variant);
+int ar_fusion_workspace_set_mode(ar_fusion_ws* ws, int mode);
+
+/* Stage rank `rank`'s partial [tokens][hidden] (device pointer `src`) into the
+ * workspace, standing in for the one-shot push of
+ * allreduce_fusion_kernel_oneshot_lamport (on one GPU nothing is pushed over
+ * NVLink; the bytes are copied by a kernel).
+ *   mode AR_MODE_LAMPORT: into the current slot (lamport_flag % 3, read on the
+ *     device) at rank * tokens * hidden elements; every 32-bit word equal to
+ *     the -0.0f sentinel (0x80000000) is written as +0.0f.
+ *   mode AR_MODE_BUFFER: into the buffer region at rank * max_token_num *
+ *     hidden elements, unchanged.
+ *   mode AR_MODE_AUTO: LAMPORT if tokens <= AR_ONESHOT_MAX_TOKENS, else BUFFER
+ *     (or the mode forced with ar_fusion_workspace_set_mode).
+ * Errors: AR_ERR_INVALID (rank, pointer, mode), AR_ERR_CAPACITY. */
+int ar_fusion_workspace_stage(ar_fusion_ws* ws, int rank, const void* src, int tokens, int mode,
+                              void* stream);
+
+/* ---------------------------------------------------------- fused call -- */
+
+/* The fused epilogue (allreduce_fusion_op, TensorRT-LLM allReduceFusionKernels.cu).
+ *   ws            workspace (status word; staged partials when partials == NULL)
+ *   partials      host array of `nranks` device pointers, each [tokens][hidden] D
+ *                 (read only), or NULL to read the partials staged in `ws`
+ *                 (AR_MODE_AUTO unless forced: Lamport slot for tokens <=
+ *                 AR_ONESHOT_MAX_TOKENS, else buffer region)
+ *   nranks        R, 1..AR_MAX_RANKS; must equal tp_size when partials == NULL
+ *   tokens        rows, >= 0 (0: nothing launched, AR_OK)
+ *   hidden_dim    row length, multiple of 8 (of 16 with AR_QUANT_NVFP4),
+ *                 <= AR_MAX_HIDDEN; must equal the workspace's when staged
+ *   dtype         enum ar_dtype; must equal the workspace's
+ *   residual_in   [tokens][hidden] D
+ *   gamma         [hidden] D
+ *   eps           RMSNorm epsilon (fp32)
+ *   pattern       one of the four valid ar_pattern combinations
+ *   residual_out  [tokens][hidden] D, written if AR_RESIDUAL_OUT, else ignored
+ *   norm_out      [tokens][hidden] D, written if AR_NORM_OUT, else ignored
+ *   quant_out     AR_QUANT_FP8: [tokens][hidden] E4M3 bytes;
+ *                 AR_QUANT_NVFP4: [tokens][hidden/2] bytes, element 2k in the
+ *                 low nibble of byte k
+ *   scale_out     AR_QUANT_NVFP4: [tokens][hidden/16] E4M3 block-scale bytes
+ *                 (row-major, linear); ignored otherwise
+ *   scale_factor  device fp32 scalar: AR_QUANT_FP8: the multiplier 1/scale;
+ *                 AR_QUANT_NVFP4: the global encode scale gs (block scale =
+ *                 E4M3(gs * blockmax / 6), codes = E2M1(n * gs / blockscale))
+ *   stream        CUDA stream
+ * Errors (before any launch): AR_ERR_INVALID (null / misaligned pointers, bad
+ * pattern, hidden not a multiple of 8 / 16, dtype or hidden mismatch),
+ * AR_ERR_UNSUPPORTED (nranks outside 1..16, hidden too large),
+ * AR_ERR_CAPACITY (staged and tokens > max_token_num), AR_ERR_CUDA (launch).
+ * Device-side: a Lamport-mode wait that gives up sets AR_ERR_TIMEOUT in the
+ * status word; outputs of that call are then undefined. */
+int ar_fusion_run(ar_fusion_ws* ws, const void* const* partials, int nranks, int tokens,
+                  int hidden_dim, int dtype, const void* residual_in, const void* gamma,
+                  float eps, int pattern, void* residual_out, void* norm_out, void* quant_out,
+                  void* scale_out, const float* scale_factor, void* stream);
+
+/* Calibration pass for the per-tensor quantisers: the same sum, residual add
+ * and RMSNorm as ar_fusion_run, writing only amax = max |n| over the whole
+ * tensor to the device fp32 *amax_out (overwritten).  Reads caller partials,
+ * or the buffer region when partials == NULL (never the Lamport slots, whose
+ * state it leaves alone).  Same argument rules as ar_fusion_run. */
+int ar_fusion_norm_amax(ar_fusion_ws* ws, const void* const* partials, int nranks, int tokens,
+                        int hidden_dim, int dtype, const void* residual_in, const void* gamma,
+                        float eps, float* amax_out, void* stream);
+
+/* ---------------------------------------------------------- plain sum -- */
+
+/* out[i] = round_D(in_0[i] + ... + in_{R-1}[i]) in fp32, rank order, for i < n
+ * (mscclpp allreduce.cu vectorSum, accumulating in fp32).
+ *   bufs    host array of `nranks` device pointers, n elements of D each
+ *   nranks  1..AR_MAX_RANKS;  n any size (no alignment tail restriction)
+ *   out     n elements of D; may alias none of the inputs
+ * Pointers need only element alignment here; 16-byte aligned inputs take the
+ * 128-bit path.  Errors: AR_ERR_INVALID, AR_ERR_UNSUPPORTED, AR_ERR_CUDA. */
+int ar_fusion_sum(const void* const* bufs, int nranks, size_t n, int dtype, void* out,
+                  void* stream);
+
+/* ---------------------------------------------------------- utilities -- */
+
+/* Message for the last failed call on this thread ("" if none). */
+const char* ar_fusion_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int ar_fusion_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AR_FUSION_H */

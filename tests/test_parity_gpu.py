@@ -1,0 +1,382 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle on the
+same seeded inputs, element by element.  Needs a GPU (marked ``gpu``)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import parity as PY
+from allreduce_residual_rmsnorm_gb300 import binding as B
+from allreduce_residual_rmsnorm_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def make_ws(w, max_tokens=None, mem=False):
+    maxT = max_tokens or max(w.T, 1)
+    if mem:
+        n = B.ar_fusion_workspace_bytes(w.R, maxT, w.H, PY.BDT[w.dtype])
+        buf = torch.empty(n, dtype=torch.uint8, device="cuda")
+        return B.ar_fusion_workspace_create(w.R, maxT, w.H, PY.BDT[w.dtype], device_mem=buf)
+    return B.ar_fusion_workspace_create(w.R, maxT, w.H, PY.BDT[w.dtype])
+
+
+def run_and_check(w, variant=B.AR_VARIANT_AUTO, staged=False, mode=B.AR_MODE_AUTO, inp=None,
+                  max_tokens=None):
+    inp = inp or W.make_fused_inputs(w)
+    ws = make_ws(w, max_tokens)
+    B.ar_fusion_workspace_set_variant(ws, variant)
+    B.ar_fusion_workspace_set_mode(ws, mode)
+    lam = staged and (mode == B.AR_MODE_LAMPORT or
+                      (mode == B.AR_MODE_AUTO and w.T <= B.AR_ONESHOT_MAX_TOKENS))
+    exp = PY.oracle_expected(w, inp, lamport_flip=lam)
+    got = PY.run_gpu(ws, w, inp, scale=exp.get("scale"), staged=staged)
+    rc, detail = B.ar_fusion_workspace_status(ws)
+    assert rc == 0, (rc, detail)
+    stats = PY.check_all(w, got, exp)
+    B.ar_fusion_workspace_destroy(ws)
+    return stats, got, exp
+
+
+# ------------------------------------------------------------ the five targets
+
+@pytest.mark.parametrize("variant", [B.AR_VARIANT_AUTO, B.AR_VARIANT_WARP_ROW, B.AR_VARIANT_CTA_ROW])
+@pytest.mark.parametrize("staged", [False, True])
+def test_tiny_r2_t16_h512(variant, staged):
+    stats, _, _ = run_and_check(W.TINY, variant, staged)
+    assert stats["residual_mismatch"] == 0 and stats["norm_mismatch"] == 0, stats
+
+
+@pytest.mark.parametrize("staged", [False, True])
+def test_decode_r8_t128_h4096(staged):
+    stats, _, _ = run_and_check(W.DECODE, B.AR_VARIANT_AUTO, staged)
+    assert stats["residual_mismatch"] == 0 and stats["norm_mismatch"] == 0, stats
+
+
+@pytest.mark.parametrize("variant", [B.AR_VARIANT_AUTO, B.AR_VARIANT_CTA_ROW, B.AR_VARIANT_BULK_PIPE])
+def test_fp8_r4_t2048_h8192(variant):
+    stats, _, _ = run_and_check(W.FP8_PREFILL, variant, staged=True)
+    assert stats["residual_mismatch"] == 0, stats
+    assert stats["norm_mismatch"] <= 0.00001 * W.FP8_PREFILL.T * W.FP8_PREFILL.H, stats
+
+
+@pytest.mark.parametrize("variant,staged", [(B.AR_VARIANT_AUTO, True),
+                                            (B.AR_VARIANT_CTA_ROW, False)])
+def test_nvfp4_r8_t8192_h7168_full_size(variant, staged):
+    # the benchmarked configuration, element by element over every output
+    stats, _, _ = run_and_check(W.NVFP4_PREFILL, variant, staged)
+    assert stats["residual_mismatch"] == 0, stats
+
+
+def test_nvfp4_with_norm_out_small():
+    w = W.NVFP4_PREFILL.with_(T=300, pattern=W.RES_NORM_NVFP4)
+    for variant in (B.AR_VARIANT_CTA_ROW, B.AR_VARIANT_BULK_PIPE):
+        stats, _, _ = run_and_check(w, variant)
+        assert stats["residual_mismatch"] == 0 and stats["norm_mismatch"] == 0, stats
+
+
+# ------------------------------------------------------------------ edges
+
+EDGE = [
+    # (R, T, H, dtype, pattern)
+    (1, 1, 8, "bf16", W.RES_NORM), (3, 5, 24, "bf16", W.NORM), (5, 3, 16, "fp16", W.RES_QUANT_NVFP4),
+    (16, 7, 520, "bf16", W.RES_NORM_FP8), (2, 37, 1000, "fp16", W.RES_QUANT_FP8),
+    (7, 9, 1024, "bf16", W.RES_NORM_NVFP4), (4, 13, 1032, "bf16", W.RES_NORM),
+    (8, 33, 2048, "fp16", W.RES_NORM), (6, 17, 7176, "bf16", W.RES_NORM_FP8),
+    (2, 3, 32768, "bf16", W.RES_QUANT_NVFP4), (16, 2, 32768, "fp16", W.RES_NORM),
+    (8, 200, 4096, "bf16", W.RES_NORM_NVFP4), (1, 500, 7168, "fp16", W.RES_QUANT_FP8),
+]
+
+
+@pytest.mark.parametrize("R,T,H,dtype,pattern", EDGE)
+@pytest.mark.parametrize("variant", [B.AR_VARIANT_AUTO, B.AR_VARIANT_WARP_ROW, B.AR_VARIANT_CTA_ROW,
+                                     B.AR_VARIANT_BULK_PIPE])
+def test_edge_shapes(R, T, H, dtype, pattern, variant):
+    w = W.FusedWorkload(f"edge_{R}_{T}_{H}", R=R, T=T, H=H, dtype=dtype, pattern=pattern,
+                        eps=1e-5, seed=R * 1000 + T)
+    stats, _, _ = run_and_check(w, variant)
+    assert stats.get("residual_mismatch", 0) == 0, stats
+    assert stats.get("norm_mismatch", 0) <= max(1, T * H // 100000), stats
+
+
+@pytest.mark.parametrize("staged", [False, True])
+def test_staged_buffer_mode_and_capacity(staged):
+    w = W.DECODE.with_(T=100)
+    stats, _, _ = run_and_check(w, B.AR_VARIANT_CTA_ROW, staged, mode=B.AR_MODE_BUFFER,
+                                max_tokens=160)
+    assert stats["residual_mismatch"] == 0
+
+
+def test_zero_tokens_launches_nothing():
+    w = W.TINY
+    ws = make_ws(w)
+    X = torch.empty(0, w.H, dtype=torch.bfloat16, device="cuda")
+    G = torch.ones(w.H, dtype=torch.bfloat16, device="cuda")
+    B.ar_fusion_run(ws, None, X, G, 1e-6, B.PATTERNS[w.pattern])
+    B.ar_fusion_run(ws, [X, X], X, G, 1e-6, B.PATTERNS[w.pattern])
+    st = B.ar_fusion_workspace_copy_state(ws)
+    assert st["calls"] == 0 and st["lamport_flag"] == 0
+    B.ar_fusion_workspace_destroy(ws)
+
+
+def test_all_zero_inputs_nvfp4_and_fp8():
+    for pat in (W.RES_NORM_NVFP4, W.RES_NORM_FP8):
+        w = W.FusedWorkload("zeros", R=4, T=6, H=256, pattern=pat)
+        inp = W.make_fused_inputs(w)
+        inp.partials.zero_()
+        inp.residual.zero_()
+        stats, got, _ = run_and_check(w, inp=inp)
+        assert np.all(got["quant"] == 0)
+        if "sf" in got:
+            assert np.all(got["sf"] == 0)
+
+
+# ------------------------------------------------------- Lamport state machine
+
+def test_lamport_sequence_state_and_retired_slot_clear():
+    w = W.TINY
+    ws = make_ws(w, mem=True)
+    info = B.ar_fusion_workspace_info(ws)
+    mem = ws.mem
+    slot_b = info["lamport_comm_bytes"]
+    lam_off = info["lamport"] - info["base"]
+    flag = 0
+    clear = 0
+    for k in range(7):
+        wk = w.with_(seed=100 + k, T=w.T - (k % 3))      # varying T changes clear sizes
+        inp = W.make_fused_inputs(wk)
+        exp = PY.oracle_expected(wk, inp, lamport_flip=True)
+        got = PY.run_gpu(ws, wk, inp, staged=True)
+        PY.check_all(wk, got, exp)
+        assert np.array_equal(got["residual"], exp["residual"])
+        st = B.ar_fusion_workspace_copy_state(ws)
+        new_flag, new_clear, rd, cl = oracle.lamport_step(flag, clear, wk.R, wk.T, wk.H)
+        assert st["lamport_flag"] == new_flag and st["clear_size"] == new_clear
+        assert st["counter"] == 0 and st["calls"] == k + 1 and st["status"] == 0
+        # the slot cleared by this call holds sentinel words over the previous clear size
+        words = mem[lam_off + cl * slot_b: lam_off + cl * slot_b + clear * 2].view(torch.int32)
+        assert bool((words == torch.tensor(-2 ** 31, dtype=torch.int32, device="cuda")).all())
+        flag, clear = new_flag, new_clear
+    B.ar_fusion_workspace_destroy(ws)
+
+
+def test_lamport_sentinel_pairs_are_flipped_on_stage():
+    w = W.TINY.with_(seed=5)
+    inp = W.make_fused_inputs(w)
+    p16 = inp.partials.view(torch.int16)
+    p16[:, :, 0] = 0                       # (lo=+0, hi=-0): the -0.0f sentinel word
+    p16[:, :, 1] = -32768
+    p16[:, 3, 4] = -32768                  # low half -0 with a non-zero high half: kept
+    stats, _, _ = run_and_check(w, staged=True, inp=inp)
+    assert stats["residual_mismatch"] == 0
+    stats, _, _ = run_and_check(w, staged=False, inp=inp)
+    assert stats["residual_mismatch"] == 0
+
+
+def test_lamport_wait_times_out_and_reset_recovers():
+    w = W.TINY
+    inp = W.make_fused_inputs(w)
+    ws = make_ws(w)
+    B.ar_fusion_workspace_set_timeout_ns(ws, 20_000_000)   # 20 ms bound per wait
+    P = inp.partials.cuda()
+    X, G = inp.residual.cuda(), inp.gamma.cuda()
+    res, nrm = torch.empty_like(X), torch.empty_like(X)
+    for r in range(w.R - 1):                # the last rank never arrives
+        B.ar_fusion_workspace_stage(ws, r, P[r])
+    B.ar_fusion_run(ws, None, X, G, w.eps, B.PATTERNS[w.pattern], residual_out=res, norm_out=nrm)
+    rc, detail = B.ar_fusion_workspace_status(ws)
+    assert rc == B.AR_ERR_TIMEOUT
+    assert detail % 32 == w.R - 1 and 0 <= detail // 32 < w.T
+    B.ar_fusion_workspace_reset(ws)
+    assert B.ar_fusion_workspace_status(ws)[0] == 0
+    got = PY.run_gpu(ws, w, inp, staged=True)
+    exp = PY.oracle_expected(w, inp, lamport_flip=True)
+    PY.check_all(w, got, exp)
+    assert B.ar_fusion_workspace_status(ws)[0] == 0
+    B.ar_fusion_workspace_destroy(ws)
+
+
+# --------------------------------------------------------------- ABI errors
+
+def test_abi_errors_launch_nothing():
+    w = W.TINY
+    ws = make_ws(w)
+    X = torch.randn(w.T, w.H, device="cuda").to(torch.bfloat16)
+    G = torch.ones(w.H, dtype=torch.bfloat16, device="cuda")
+    P = [torch.randn(w.T, w.H, device="cuda").to(torch.bfloat16) for _ in range(w.R)]
+    out = torch.full((w.T, w.H), 7.0, dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros(w.T, w.H, dtype=torch.uint8, device="cuda")
+    sc = torch.ones(1, device="cuda")
+    L = B.lib()
+
+    def expect(code, fn):
+        with pytest.raises(B.ArFusionError) as e:
+            fn()
+        assert e.value.code == code, (e.value, code)
+
+    expect(B.AR_ERR_INVALID, lambda: B.ar_fusion_run(ws, P, X, G, 1e-6, 0, out, out))
+    expect(B.AR_ERR_INVALID, lambda: B.ar_fusion_run(ws, P, X, G, 1e-6, B.AR_RESIDUAL_OUT, out, out))
+    expect(B.AR_ERR_INVALID, lambda: B.ar_fusion_run(ws, P, X, G, 1e-6, B.AR_NORM_OUT | B.AR_QUANT_FP8,
+                                                     out, out, q, None, sc))
+    expect(B.AR_ERR_INVALID, lambda: B.ar_fusion_run(ws, P, X, G, 1e-6,
+                                                     B.AR_RESIDUAL_OUT | B.AR_QUANT_FP8 | B.AR_QUANT_NVFP4,
+                                                     out, out, q, q, sc))
+    expect(B.AR_ERR_INVALID, lambda: B.ar_fusion_run(ws, P, X, G, 1e-6, 16 | B.AR_NORM_OUT, out, out))
+    expect(B.AR_ERR_INVALID, lambda: B.ar_fusion_run(ws, P, X, G, 1e-6, B.PATTERNS["res_fp8"], out,
+                                                     None, q, None, None))
+    expect(B.AR_ERR_INVALID, lambda: B.ar_fusion_run(ws, P, X, G, 1e-6, B.PATTERNS["res_nvfp4"], out,
+                                                     None, q, None, sc))
+    expect(B.AR_ERR_INVALID, lambda: B.ar_fusion_run(ws, P, X, G, 1e-6, B.PATTERNS["res_norm"], None, out))
+    # misaligned pointer
+    Xo = torch.empty(w.T * w.H + 8, dtype=torch.bfloat16, device="cuda")[1:1 + w.T * w.H].view(w.T, w.H)
+    expect(B.AR_ERR_INVALID, lambda: B.ar_fusion_run(ws, P, Xo, G, 1e-6, B.PATTERNS["res_norm"], out, out))
+    # dtype mismatch with the workspace
+    Xh = X.half()
+    expect(B.AR_ERR_INVALID, lambda: B.ar_fusion_run(ws, [p.half() for p in P], Xh, G.half(), 1e-6,
+                                                     B.PATTERNS["res_norm"], out.half(), out.half()))
+    # staged: wrong rank count, capacity
+    expect(B.AR_ERR_INVALID, lambda: B.ar_fusion_run(ws, None, X, G, 1e-6, B.PATTERNS["res_norm"],
+                                                     out, out, nranks=3))
+    Xbig = torch.randn(w.T + 1, w.H, device="cuda").to(torch.bfloat16)
+    outbig = torch.empty_like(Xbig)
+    expect(B.AR_ERR_CAPACITY, lambda: B.ar_fusion_run(ws, None, Xbig, G, 1e-6, B.PATTERNS["res_norm"],
+                                                      outbig, outbig))
+    expect(B.AR_ERR_UNSUPPORTED, lambda: B.ar_fusion_run(ws, P * 9, X, G, 1e-6, B.PATTERNS["res_norm"],
+                                                         out, out))
+    expect(B.AR_ERR_CAPACITY, lambda: B.ar_fusion_workspace_stage(ws, 0, Xbig))
+    expect(B.AR_ERR_INVALID, lambda: B.ar_fusion_workspace_stage(ws, w.R, X))
+    # NVFP4 needs hidden % 16 == 0
+    ws2 = B.ar_fusion_workspace_create(2, 4, 24, B.AR_DT_BF16)
+    X24 = torch.zeros(4, 24, dtype=torch.bfloat16, device="cuda")
+    G24 = torch.ones(24, dtype=torch.bfloat16, device="cuda")
+    expect(B.AR_ERR_INVALID, lambda: B.ar_fusion_run(ws2, [X24, X24], X24, G24, 1e-6, B.PATTERNS["res_nvfp4"],
+                                                     X24, None, q, q, sc))
+    torch.cuda.synchronize()
+    assert bool((out == 7.0).all()), "a rejected call wrote an output"
+    st = B.ar_fusion_workspace_copy_state(ws)
+    assert st["calls"] == 0
+    del L
+    B.ar_fusion_workspace_destroy(ws2)
+    B.ar_fusion_workspace_destroy(ws)
+
+
+def test_outputs_stay_inside_their_bounds():
+    # canary bands around every output in place of a memory checker
+    w = W.FusedWorkload("canary", R=3, T=37, H=1040, pattern=W.RES_NORM_NVFP4, seed=3)
+    inp = W.make_fused_inputs(w)
+    exp = PY.oracle_expected(w, inp)
+    for variant in (B.AR_VARIANT_WARP_ROW, B.AR_VARIANT_CTA_ROW, B.AR_VARIANT_BULK_PIPE):
+        ws = make_ws(w)
+        B.ar_fusion_workspace_set_variant(ws, variant)
+        pad = 4096
+        def band(n, dt):
+            t = torch.full((n + 2 * pad,), 0x5A if dt == torch.uint8 else 1234.0, dtype=dt, device="cuda")
+            return t, t[pad:pad + n]
+        rb, res = band(w.T * w.H, torch.bfloat16)
+        nb, nrm = band(w.T * w.H, torch.bfloat16)
+        qb, q = band(w.T * w.H // 2, torch.uint8)
+        sb, s = band(w.T * w.H // 16, torch.uint8)
+        sc = torch.tensor([exp["scale"]], device="cuda")
+        P = inp.partials.cuda()
+        B.ar_fusion_run(ws, [P[r] for r in range(w.R)], inp.residual.cuda(), inp.gamma.cuda(), w.eps,
+                        B.PATTERNS[w.pattern], res.view(w.T, w.H), nrm.view(w.T, w.H), q, s, sc)
+        torch.cuda.synchronize()
+        for full, dt in ((rb, torch.bfloat16), (nb, torch.bfloat16), (qb, torch.uint8), (sb, torch.uint8)):
+            v = 0x5A if dt == torch.uint8 else 1234.0
+            assert bool((full[:pad] == v).all()) and bool((full[-pad:] == v).all()), variant
+        got = {"residual": W.bits(res.view(w.T, w.H).cpu()), "norm": W.bits(nrm.view(w.T, w.H).cpu()),
+               "quant": q.view(w.T, -1).cpu().numpy(), "sf": s.view(w.T, -1).cpu().numpy()}
+        PY.check_all(w, got, exp)
+        B.ar_fusion_workspace_destroy(ws)
+
+
+# ------------------------------------------- encoders over every bf16 value
+
+def _gamma_probe(gamma_vals, pattern, scale, sign_seed=0):
+    """A row of |y| = 1 with eps = 0 has rstd = 1, so n = sign * gamma exactly:
+    gamma then carries the values the quantiser sees."""
+    H = gamma_vals.numel()
+    T = 2
+    rng = torch.Generator().manual_seed(sign_seed)
+    sign = torch.where(torch.rand(T, H, generator=rng) < 0.5, -1.0, 1.0)
+    w = W.FusedWorkload("probe", R=1, T=T, H=H, eps=0.0, pattern=pattern)
+    inp = W.FusedInputs(partials=sign.to(torch.bfloat16).unsqueeze(0).contiguous(),
+                        residual=torch.zeros(T, H, dtype=torch.bfloat16),
+                        gamma=gamma_vals.to(torch.bfloat16), eps=0.0)
+    ws = make_ws(w)
+    B.ar_fusion_workspace_set_variant(ws, B.AR_VARIANT_CTA_ROW)
+    got = PY.run_gpu(ws, w, inp, scale=scale)
+    B.ar_fusion_workspace_destroy(ws)
+    n = W.bits((sign * gamma_vals.to(torch.bfloat16).float()).to(torch.bfloat16))
+    assert np.array_equal(got["norm"], n)
+    return got, n
+
+
+@pytest.mark.parametrize("mult", [1.0, 0.5, 448.0 / 7.0, 2.0 ** -9])
+def test_fp8_encoder_every_bf16_value(mult):
+    allbits = torch.arange(0, 65536, dtype=torch.int32)
+    finite = ((allbits >> 7) & 0xff) != 0xff
+    vals = allbits[finite].to(torch.int16).view(torch.bfloat16)
+    vals = torch.cat([vals, torch.zeros((-vals.numel()) % 32768, dtype=torch.bfloat16)])
+    for chunk in vals.split(32768):
+        got, n = _gamma_probe(chunk, W.RES_NORM_FP8, mult)
+        exp = oracle.quant_fp8(oracle.BF16, n, np.float32(mult))
+        assert np.array_equal(got["quant"], exp)
+
+
+def test_nvfp4_encoder_many_values():
+    g = torch.Generator().manual_seed(1)
+    e = torch.rand(32768, generator=g) * 40 - 20
+    vals = (torch.exp2(e) * torch.where(torch.rand(32768, generator=g) < 0.5, -1.0, 1.0))
+    vals[::97] = 0.0
+    for gs in (1.0, 2688.0 / 37.5, 3.0e5):
+        got, n = _gamma_probe(vals, W.RES_NORM_NVFP4, gs)
+        eq, es = oracle.quant_nvfp4(oracle.BF16, n, np.float32(gs))
+        assert np.array_equal(got["sf"], es)
+        assert np.array_equal(got["quant"], eq)
+
+
+# -------------------------------------------------------------- calibration
+
+def test_norm_amax_matches_oracle():
+    for w in (W.FP8_PREFILL.with_(T=256), W.TINY):
+        inp = W.make_fused_inputs(w)
+        exp = PY.oracle_expected(w.with_(pattern=W.RES_NORM_FP8), inp)
+        ws = make_ws(w)
+        P = inp.partials.cuda()
+        amax = torch.full((1,), -1.0, device="cuda")
+        B.ar_fusion_norm_amax(ws, [P[r] for r in range(w.R)], inp.residual.cuda(), inp.gamma.cuda(),
+                              w.eps, amax)
+        torch.cuda.synchronize()
+        assert float(amax.item()) == exp["amax"]
+        B.ar_fusion_workspace_destroy(ws)
+
+
+# ---------------------------------------------------------------- plain sum
+
+@pytest.mark.parametrize("N", W.SUM_SIZES)
+def test_vector_sum_sizes(N):
+    w = W.SumWorkload(f"sum{N}", R=8, N=N)
+    x = W.make_sum_inputs(w)
+    exp = oracle.vector_sum(oracle.FP16, W.bits(x))
+    xd = x.cuda()
+    out = torch.full((N,), float("nan"), dtype=torch.float16, device="cuda")
+    B.ar_fusion_sum([xd[r] for r in range(w.R)], out)
+    torch.cuda.synchronize()
+    got = W.bits(out.cpu())
+    assert np.array_equal(got, exp), np.count_nonzero(got != exp)
+
+
+@pytest.mark.parametrize("R,N,dtype,offset", [(1, 1000, "fp16", 0), (3, 4099, "bf16", 0),
+                                               (16, 77777, "fp16", 0), (5, 12345, "bf16", 1),
+                                               (2, 7, "fp16", 3)])
+def test_vector_sum_ranks_types_and_misaligned(R, N, dtype, offset):
+    x = W.make_sum_inputs(W.SumWorkload("s", R=R, N=N + offset, dtype=dtype))
+    exp = oracle.vector_sum(PY.ODT[dtype], W.bits(x[:, offset:]))
+    xd = x.cuda()
+    out_full = torch.zeros(N + 8, dtype=xd.dtype, device="cuda")
+    out = out_full[offset:offset + N]
+    B.ar_fusion_sum([xd[r, offset:] for r in range(R)], out)
+    torch.cuda.synchronize()
+    assert np.array_equal(W.bits(out.cpu()), exp)
+    assert bool((out_full[offset + N:] == 0).all())
