@@ -157,24 +157,47 @@ struct DF {
     float hi, lo;
 };
 
-__device__ __forceinline__ void df_add_term(DF& a, float t)
+// IEEE round-to-nearest fp32 addition on either side (no contraction: there
+// is no multiply to fuse with).
+__host__ __device__ __forceinline__ float rn_add(float a, float b)
 {
-    float s = __fadd_rn(a.hi, t);
-    float bb = __fadd_rn(s, -a.hi);
-    float err = __fadd_rn(__fadd_rn(a.hi, -__fadd_rn(s, -bb)), __fadd_rn(t, -bb));
-    a.hi = s;
-    a.lo = __fadd_rn(a.lo, err);
+#ifdef __CUDA_ARCH__
+    return __fadd_rn(a, b);
+#else
+    return a + b;
+#endif
 }
 
-__device__ __forceinline__ DF df_add(DF a, DF b)
+// TwoSum: s + err == a + b exactly.
+__host__ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& err)
 {
-    float s = __fadd_rn(a.hi, b.hi);
-    float bb = __fadd_rn(s, -a.hi);
-    float err = __fadd_rn(__fadd_rn(a.hi, -__fadd_rn(s, -bb)), __fadd_rn(b.hi, -bb));
-    float lo = __fadd_rn(__fadd_rn(a.lo, b.lo), err);
-    float hi = __fadd_rn(s, lo);
-    lo = __fadd_rn(lo, -__fadd_rn(hi, s));
-    return DF{hi, lo};
+    s = rn_add(a, b);
+    const float bb = rn_add(s, -a);
+    err = rn_add(rn_add(a, -rn_add(s, -bb)), rn_add(b, -bb));
+}
+
+__host__ __device__ __forceinline__ void df_add_term(DF& a, float t)
+{
+    float s, err;
+    two_sum(a.hi, t, s, err);
+    a.hi = s;
+    a.lo = rn_add(a.lo, err);
+}
+
+__host__ __device__ __forceinline__ DF df_add(DF a, DF b)
+{
+    float s, err;
+    two_sum(a.hi, b.hi, s, err);
+    const float lo = rn_add(rn_add(a.lo, b.lo), err);
+    // renormalise: hi + lo2 == s + lo exactly (|s| >= |lo|)
+    const float hi = rn_add(s, lo);
+    const float lo2 = rn_add(lo, -rn_add(hi, -s));
+    return DF{hi, lo2};
+}
+
+__host__ __device__ __forceinline__ float df_round(DF a)
+{
+    return rn_add(a.hi, a.lo);
 }
 
 __device__ __forceinline__ DF df_shfl_xor(DF a, int m)

@@ -204,7 +204,7 @@ fused_rows_kernel(const FusedArgs a)
             ss = tot;
             parity ^= 1;
         }
-        const float ss32 = __fadd_rn(ss.hi, ss.lo);
+        const float ss32 = df_round(ss);
         const float ms = __fdiv_rn(ss32, (float)H);
         const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, a.eps)));
 

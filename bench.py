@@ -43,6 +43,9 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=None)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--variant", default="auto", choices=["auto", "cta", "pipe", "warp"])
+    p.add_argument("--tokens", type=int, default=None,
+                   help="smaller token count (profiling captures); default: the full workload")
+    p.add_argument("--no-e2e", action="store_true")
     return p.parse_args()
 
 
@@ -229,6 +232,8 @@ def main():
     args = parse()
     from allreduce_residual_rmsnorm_gb300 import workloads as W
     w = W.NVFP4_PREFILL
+    if args.tokens:
+        w = w.with_(T=args.tokens, name=f"{w.name}_t{args.tokens}")
     if args.impl == "reference":
         run_reference(args, w)
         return
@@ -269,7 +274,8 @@ def main():
     amax = torch.empty(1, dtype=torch.float32, device=dev)
     B.ar_fusion_norm_amax(ws, None, X, G, w.eps, amax)
     torch.cuda.synchronize(dev)
-    gs = torch.tensor([2688.0 / float(amax.item())], dtype=torch.float32, device=dev)
+    a = float(amax.item())
+    gs = torch.tensor([2688.0 / a if a > 0 else 1.0], dtype=torch.float32, device=dev)
     pattern = B.PATTERNS[w.pattern]
 
     def step():
@@ -313,7 +319,7 @@ def main():
         total_ms = float(t.item())
 
     # ---- end to end: pinned host inputs -> device, run, outputs -> host
-    e2e_steps = args.e2e_steps or max(3, min(args.steps, 10))
+    e2e_steps = 0 if args.no_e2e else (args.e2e_steps or max(3, min(args.steps, 10)))
     Ph = inp["P"].pin_memory()
     Xh = inp["X"].pin_memory()
     Pd = torch.empty_like(P)
@@ -331,7 +337,8 @@ def main():
         q_h.copy_(q, non_blocking=True)
         sf_h.copy_(sf, non_blocking=True)
 
-    e2e_step()
+    if e2e_steps:
+        e2e_step()
     torch.cuda.synchronize(dev)
     if pg:
         pg.barrier()
@@ -386,8 +393,8 @@ def main():
                      "peak_kind": f"{peak_kind} (hbm_gbs, copy bandwidth)",
                      "algorithmic_bytes_per_launch": bytes_alg,
                      "avg_launch_us": avg_launch_s * 1e6},
-        "e2e": {"value": world * T * e2e_steps / (e2e_ms / 1e3), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": ({"value": world * T * e2e_steps / (e2e_ms / 1e3), "unit": "tokens/s",
+                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h} if e2e_steps else None),
         "gpu_launches": args.steps,
         "clocks": clk,
     }
