@@ -291,9 +291,13 @@ float oracle_amax(int dtype, const uint16_t* x, int64_t n)
 }
 
 /* Per-tensor FP8 scale convention of the target configuration: the scale is
- * amax / 448 and the kernel multiplies by its inverse, computed once. */
+ * amax / 448 and the kernel multiplies by its inverse, computed once.  An
+ * all-zero tensor has no amax to map; it gets the multiplier 1.0 (every code
+ * is then 0) instead of an infinite one. */
 float oracle_fp8_inv_scale(float amax)
 {
+    if (!(amax > 0.0f))
+        return 1.0f;
     float scale = amax / 448.0f;
     return 1.0f / scale;
 }

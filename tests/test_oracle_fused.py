@@ -240,6 +240,16 @@ def test_fp8_amax_element_maps_to_448_and_roundtrip_bound():
 
 # ------------------------------------------------------------------ NVFP4
 
+def test_scales_of_an_all_zero_tensor_are_finite():
+    # an all-zero tensor (amax = 0) must not produce an infinite multiplier
+    assert oracle.fp8_inv_scale(0.0) == 1.0
+    assert oracle.nvfp4_global_scale(0.0) == 1.0
+    z = np.zeros((2, 32), np.uint16)
+    assert np.all(oracle.quant_fp8(BF16, z, oracle.fp8_inv_scale(0.0)) == 0)
+    q, s = oracle.quant_nvfp4(BF16, z, oracle.nvfp4_global_scale(0.0))
+    assert np.all(q == 0) and np.all(s == 0)
+
+
 def test_nvfp4_zero_block_and_max_element():
     H = 64
     n = np.zeros((2, H), np.uint16)
