@@ -314,8 +314,6 @@ int pick_variant(const ar_fusion_ws* ws, const FusedArgs& a)
         v = AR_VARIANT_AUTO;
     if (v != AR_VARIANT_AUTO)
         return v;
-    if (!a.lamport && fused_pipe_supported(ws->dtype, a.H, a.R) && a.T >= 2 * ws->sms)
-        return AR_VARIANT_BULK_PIPE;
     return a.H <= 1024 ? AR_VARIANT_WARP_ROW : AR_VARIANT_CTA_ROW;
 }
 
