@@ -86,6 +86,66 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8])
     return v;
 }
 
+// ------------------------------------------- mixed-precision accumulation
+//
+// add.rn.f32.{bf16,f16}: d = f(a) + c rounded once to fp32 -- the same value as
+// unpacking a and adding, in one instruction.  Addition commutes exactly, so
+// s + f(P_r) keeps the rank order of the fp32 sum.
+
+template <class D>
+__device__ __forceinline__ void add2(float& lo, float& hi, uint32_t w);
+
+template <>
+__device__ __forceinline__ void add2<Bf16>(float& lo, float& hi, uint32_t w)
+{
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "add.rn.f32.bf16 %0, l, %0;\n\tadd.rn.f32.bf16 %1, h, %1;\n\t}"
+        : "+f"(lo), "+f"(hi)
+        : "r"(w));
+}
+
+template <>
+__device__ __forceinline__ void add2<Fp16>(float& lo, float& hi, uint32_t w)
+{
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "add.rn.f32.f16 %0, l, %0;\n\tadd.rn.f32.f16 %1, h, %1;\n\t}"
+        : "+f"(lo), "+f"(hi)
+        : "r"(w));
+}
+
+// s[i] = s[i] + f(v_i), i < 8
+template <class D>
+__device__ __forceinline__ void add8(float (&s)[8], const uint4& v)
+{
+    add2<D>(s[0], s[1], v.x);
+    add2<D>(s[2], s[3], v.y);
+    add2<D>(s[4], s[5], v.z);
+    add2<D>(s[6], s[7], v.w);
+}
+
+// Squares of a packed pair, exact (8- or 11-bit significands): fma with a
+// -0.0 addend, so a zero element gives +0.
+template <class D>
+__device__ __forceinline__ void sq2(float& lo, float& hi, uint32_t w);
+
+template <>
+__device__ __forceinline__ void sq2<Bf16>(float& lo, float& hi, uint32_t w)
+{
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, l, l, 0f80000000;\n\tfma.rn.f32.bf16 %1, h, h, 0f80000000;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(w));
+}
+
+template <>
+__device__ __forceinline__ void sq2<Fp16>(float& lo, float& hi, uint32_t w)
+{
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "fma.rn.f32.f16 %0, l, l, 0f80000000;\n\tfma.rn.f32.f16 %1, h, h, 0f80000000;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(w));
+}
+
 // ------------------------------------------------------------ memory ops
 
 // Streaming 128-bit load of data read exactly once (no L1 allocation).

@@ -1,0 +1,120 @@
+// Per-vector steps of the fused epilogue shared by every kernel variant
+// (TensorRT-LLM allReduceFusionKernels.cu: add128 / fused_op for the residual,
+// rms_norm for the normalisation, fused_op's quantised output).
+//
+// A "vector" is 8 consecutive elements of a row (16 bytes of bf16/fp16).
+#pragma once
+
+#include "ar_common.cuh"
+#include "ar_internal.h"
+
+namespace arf {
+
+// From the fp32 rank sum s of one vector and the residual x:
+//   a = rnd(s);  y = rnd(f(a) + f(x));  ss += y^2 (exact squares, TwoSum).
+// Returns y (packed).
+template <class D>
+__device__ __forceinline__ uint4 residual_vec(const float (&s)[8], const uint4& x, DF& ss)
+{
+    float a[8];
+    unpack8<D>(pack8<D>(s), a);
+    add8<D>(a, x);
+    const uint4 y = pack8<D>(a);
+    float t[8];
+    sq2<D>(t[0], t[1], y.x);
+    sq2<D>(t[2], t[3], y.y);
+    sq2<D>(t[4], t[5], y.z);
+    sq2<D>(t[6], t[7], y.w);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        df_add_term(ss, t[i]);
+    return y;
+}
+
+// rstd = 1 / sqrt(ss / H + eps), each step IEEE round-to-nearest.
+__device__ __forceinline__ float inv_rms(DF ss, int H, float eps)
+{
+    const float ms = __fdiv_rn(df_round(ss), (float)H);
+    return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+}
+
+// Combine one DF value per warp (nw <= 32 values in `slots`) in a fixed order
+// that every warp of the block reproduces bit for bit: lane l takes slot l,
+// then an xor butterfly.
+__device__ __forceinline__ DF block_combine(const DF* slots, int nw, int lane)
+{
+    DF v = lane < nw ? slots[lane] : DF{0.0f, 0.0f};
+    return df_warp_sum(v);
+}
+
+// gamma of one vector as fp32 (loaded once per kernel)
+template <class D>
+__device__ __forceinline__ void load_gamma(const uint8_t* gamma, int v, bool ok, float (&g)[8])
+{
+    if (ok) {
+        unpack8<D>(ld_keep(gamma + (size_t)v * 16), g);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            g[i] = 0.0f;
+    }
+}
+
+// n = rnd((f(y) * rstd) * gamma); stores norm_out and the quantised outputs
+// of vector v of `row`.  Every lane of the warp must call this (the NVFP4
+// block maximum is exchanged with the xor-1 neighbour); `ok` masks the stores
+// of lanes past the end of the row.
+template <class D>
+__device__ __forceinline__ void normalize_vec(const FusedArgs& a, int pat, int row, int v, bool ok,
+                                              const uint4& y, const float (&g)[8], float rstd,
+                                              float qscale, float& amax_local)
+{
+    const int H = a.H;
+    float yf[8], nf[8];
+    unpack8<D>(y, yf);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        nf[i] = __fmul_rn(__fmul_rn(yf[i], rstd), g[i]);
+    const uint4 nv = pack8<D>(nf);
+    if (ok && (pat & AR_NORM_OUT))
+        st_vec(a.norm_out + ((size_t)row * H + (size_t)v * 8) * 2, nv);
+    if (!(pat & (AR_QUANT_FP8 | AR_QUANT_NVFP4)) && !a.amax_out)
+        return;
+    float nq[8];
+    unpack8<D>(nv, nq);
+    if (a.amax_out && ok) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            amax_local = fmaxf(amax_local, fabsf(nq[i]));
+    }
+    if (pat & AR_QUANT_FP8) {
+        float t[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            t[i] = __fmul_rn(nq[i], qscale);
+        const uint2 c = e4m3x8(t);
+        if (ok)
+            st_u2(a.quant_out + (size_t)row * H + (size_t)v * 8, c.x, c.y);
+    } else if (pat & AR_QUANT_NVFP4) {
+        float bm = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            bm = fmaxf(bm, fabsf(nq[i]));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+        const uint32_t sf = e4m3_byte(__fmul_rn(qscale, __fdiv_rn(bm, 6.0f)));
+        const float dec = e4m3_to_f32(sf);
+        const float enc = dec == 0.0f ? 0.0f : __fdiv_rn(qscale, dec);
+        float t[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            t[i] = __fmul_rn(nq[i], enc);
+        const uint32_t codes = e2m1x8(t);
+        if (ok) {
+            *reinterpret_cast<uint32_t*>(a.quant_out + (size_t)row * (H / 2) + (size_t)v * 4) = codes;
+            if ((v & 1) == 0)
+                a.scale_out[(size_t)row * (H / 16) + (v >> 1)] = (uint8_t)sf;
+        }
+    }
+}
+
+}  // namespace arf

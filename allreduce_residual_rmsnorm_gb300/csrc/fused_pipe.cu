@@ -20,8 +20,7 @@
 // global timer).  A wait that gives up records AR_ERR_TIMEOUT in the
 // workspace status word, tells the block to stop, and the producer lane still
 // waits (bounded) for its copies in flight before the block exits.
-#include "ar_common.cuh"
-#include "ar_internal.h"
+#include "fused_core.cuh"
 
 #include <mutex>
 
@@ -98,6 +97,18 @@ constexpr uint32_t kSmemTail = 2048;     // barriers, reduction slots, flags
 
 }  // namespace
 
+// Ring position: stage index and the parity of its current use.
+struct Ring {
+    uint32_t s = 0, ph = 0;
+    __device__ __forceinline__ void next(uint32_t S)
+    {
+        if (++s == S) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+};
+
 template <class D, int VPT>
 __global__ void __launch_bounds__(544, 1)
 fused_pipe_kernel(const FusedArgs a, const int S, const int NC)
@@ -117,11 +128,14 @@ fused_pipe_kernel(const FusedArgs a, const int S, const int NC)
     const int lane = tid & 31;
     const int ncw = NC >> 5;
     const uint64_t tmo = a.timeout_ns;
+    const uint32_t smem0 = smem_addr(smem);
+    const uint32_t full0 = smem_addr(full);
+    const uint32_t empty0 = smem_addr(empty);
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(smem_addr(&full[s]), 1);
-            mbar_init(smem_addr(&empty[s]), (uint32_t)ncw);
+            mbar_init(full0 + 8u * s, 1);
+            mbar_init(empty0 + 8u * s, (uint32_t)ncw);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -131,14 +145,14 @@ fused_pipe_kernel(const FusedArgs a, const int S, const int NC)
     // ------------------------------------------------------------ producer
     if (warp == ncw) {
         if (lane == 0) {
-            uint32_t it = 0;
+            Ring ring;
+            uint32_t issued = 0;
             bool ok = true;
             for (int row = blockIdx.x; ok && row < a.T; row += gridDim.x) {
                 const size_t roff = (size_t)row * stage_bytes;
-                for (int u = 0; u <= R; ++u, ++it) {
-                    const uint32_t s = it % (uint32_t)S;
-                    const uint32_t n = it / (uint32_t)S;
-                    if (n > 0 && !mbar_wait(smem_addr(&empty[s]), (n - 1) & 1u, tmo)) {
+                for (int u = 0; u <= R; ++u) {
+                    // a stage's previous use must have been released by every consumer warp
+                    if (issued >= (uint32_t)S && !mbar_wait(empty0 + 8u * ring.s, ring.ph ^ 1u, tmo)) {
                         record_error(a.state, AR_ERR_TIMEOUT, -2);
                         *abort_flag = 1;
                         ok = false;
@@ -149,16 +163,26 @@ fused_pipe_kernel(const FusedArgs a, const int S, const int NC)
                         break;
                     }
                     const uint8_t* src = u < R ? a.partial[u] + roff : a.residual_in + roff;
-                    mbar_arrive_expect_tx(smem_addr(&full[s]), stage_bytes);
-                    bulk_g2s(smem_addr(smem + (size_t)s * stage_bytes), src, stage_bytes,
-                             smem_addr(&full[s]));
+                    mbar_arrive_expect_tx(full0 + 8u * ring.s, stage_bytes);
+                    bulk_g2s(smem0 + ring.s * stage_bytes, src, stage_bytes, full0 + 8u * ring.s);
+                    ++issued;
+                    ring.next((uint32_t)S);
                 }
             }
             // tail: every issued copy must have landed before the block may exit
-            const uint32_t issued = it;
-            for (uint32_t k = issued > (uint32_t)S ? issued - S : 0; k < issued; ++k) {
-                const uint32_t s = k % (uint32_t)S;
-                if (!mbar_wait(smem_addr(&full[s]), (k / (uint32_t)S) & 1u, tmo))
+            // (at most one use per stage is outstanding)
+            const uint32_t n_tail = issued < (uint32_t)S ? issued : (uint32_t)S;
+            for (uint32_t k = 0; k < n_tail; ++k) {
+                // step back k+1 positions from the next free position
+                uint32_t s = ring.s, ph = ring.ph;
+                for (uint32_t j = 0; j <= k; ++j) {
+                    if (s == 0) {
+                        s = (uint32_t)S;
+                        ph ^= 1u;
+                    }
+                    --s;
+                }
+                if (!mbar_wait(full0 + 8u * s, ph, tmo))
                     record_error(a.state, AR_ERR_TIMEOUT, -3);
             }
         }
@@ -167,53 +191,50 @@ fused_pipe_kernel(const FusedArgs a, const int S, const int NC)
 
     // ----------------------------------------------------------- consumers
     const int g = tid;
-    uint4 gv[VPT];
+    float gf[VPT][8];
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-        const int v = g + k * NC;
-        gv[k] = v < Hv ? ld_keep(a.gamma + (size_t)v * 16) : make_uint4(0, 0, 0, 0);
-    }
+    for (int k = 0; k < VPT; ++k)
+        load_gamma<D>(a.gamma, g + k * NC, g + k * NC < Hv, gf[k]);
     float qscale = 0.0f;
     if (pat & (AR_QUANT_FP8 | AR_QUANT_NVFP4))
         qscale = *a.scale_factor;
+    float amax_unused = 0.0f;
 
-    uint32_t it = 0;
+    Ring ring;
     int parity = 0;
     for (int row = blockIdx.x; row < a.T; row += gridDim.x) {
         const size_t roff = (size_t)row * stage_bytes;
         float acc[VPT][8];
         uint4 xr[VPT];
         bool ok = true;
-        for (int u = 0; u <= R; ++u, ++it) {
-            const uint32_t s = it % (uint32_t)S;
-            if (!mbar_wait(smem_addr(&full[s]), (it / (uint32_t)S) & 1u, tmo)) {
+        for (int u = 0; u <= R; ++u) {
+            if (!mbar_wait(full0 + 8u * ring.s, ring.ph, tmo)) {
                 record_error(a.state, AR_ERR_TIMEOUT, -1);
                 *abort_flag = 1;
                 ok = false;
                 break;
             }
-            const uint8_t* st = smem + (size_t)s * stage_bytes;
+            const uint8_t* st = smem + (size_t)ring.s * stage_bytes;
+            uint4 w[VPT];
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const int v = g + k * NC;
-                if (v < Hv) {
-                    const uint4 w = *reinterpret_cast<const uint4*>(st + (size_t)v * 16);
-                    if (u == R) {
-                        xr[k] = w;
-                    } else if (u == 0) {
-                        unpack8<D>(w, acc[k]);
-                    } else {
-                        float t[8];
-                        unpack8<D>(w, t);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            acc[k][i] = __fadd_rn(acc[k][i], t[i]);
-                    }
-                }
+                w[k] = v < Hv ? *reinterpret_cast<const uint4*>(st + (size_t)v * 16)
+                              : make_uint4(0, 0, 0, 0);
             }
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(smem_addr(&empty[s]));
+                mbar_arrive(empty0 + 8u * ring.s);
+            ring.next((uint32_t)S);
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                if (u == 0)
+                    unpack8<D>(w[k], acc[k]);
+                else if (u < R)
+                    add8<D>(acc[k], w[k]);
+                else
+                    xr[k] = w[k];
+            }
         }
 
         DF ss = {0.0f, 0.0f};
@@ -223,21 +244,9 @@ fused_pipe_kernel(const FusedArgs a, const int S, const int NC)
             for (int k = 0; k < VPT; ++k) {
                 const int v = g + k * NC;
                 if (v < Hv) {
-                    float af[8], xf[8];
-                    unpack8<D>(pack8<D>(acc[k]), af);
-                    unpack8<D>(xr[k], xf);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        af[i] = __fadd_rn(af[i], xf[i]);
-                    const uint4 y = pack8<D>(af);
-                    yv[k] = y;
+                    yv[k] = residual_vec<D>(acc[k], xr[k], ss);
                     if (pat & AR_RESIDUAL_OUT)
-                        st_vec(a.residual_out + roff + (size_t)v * 16, y);
-                    float yf[8];
-                    unpack8<D>(y, yf);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        df_add_term(ss, __fmul_rn(yf[i], yf[i]));
+                        st_vec(a.residual_out + roff + (size_t)v * 16, yv[k]);
                 } else {
                     yv[k] = make_uint4(0, 0, 0, 0);
                 }
@@ -249,60 +258,13 @@ fused_pipe_kernel(const FusedArgs a, const int S, const int NC)
         consumer_sync(NC);
         if (*abort_flag)
             break;
-        DF tot = red[parity * 32];
-        for (int w = 1; w < ncw; ++w)
-            tot = df_add(tot, red[parity * 32 + w]);
+        ss = block_combine(red + parity * 32, ncw, lane);
         parity ^= 1;
-        const float ss32 = df_round(tot);
-        const float ms = __fdiv_rn(ss32, (float)H);
-        const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, a.eps)));
-
+        const float rstd = inv_rms(ss, H, a.eps);
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int v = g + k * NC;
-            const bool okv = v < Hv;
-            float yf[8], gf[8], nf[8];
-            unpack8<D>(yv[k], yf);
-            unpack8<D>(gv[k], gf);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                nf[i] = __fmul_rn(__fmul_rn(yf[i], rstd), gf[i]);
-            const uint4 nv = pack8<D>(nf);
-            if (okv && (pat & AR_NORM_OUT))
-                st_vec(a.norm_out + roff + (size_t)v * 16, nv);
-            if (pat & (AR_QUANT_FP8 | AR_QUANT_NVFP4)) {
-                float nq[8];
-                unpack8<D>(nv, nq);
-                if (pat & AR_QUANT_FP8) {
-                    float t[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        t[i] = __fmul_rn(nq[i], qscale);
-                    const uint2 c = e4m3x8(t);
-                    if (okv)
-                        st_u2(a.quant_out + (size_t)row * H + (size_t)v * 8, c.x, c.y);
-                } else {
-                    float bm = 0.0f;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        bm = fmaxf(bm, fabsf(nq[i]));
-                    bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
-                    const uint32_t sf = e4m3_byte(__fmul_rn(qscale, __fdiv_rn(bm, 6.0f)));
-                    const float dec = e4m3_to_f32(sf);
-                    const float enc = dec == 0.0f ? 0.0f : __fdiv_rn(qscale, dec);
-                    float t[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        t[i] = __fmul_rn(nq[i], enc);
-                    const uint32_t codes = e2m1x8(t);
-                    if (okv) {
-                        *reinterpret_cast<uint32_t*>(a.quant_out + (size_t)row * (H / 2) +
-                                                     (size_t)v * 4) = codes;
-                        if ((v & 1) == 0)
-                            a.scale_out[(size_t)row * (H / 16) + (v >> 1)] = (uint8_t)sf;
-                    }
-                }
-            }
+            normalize_vec<D>(a, pat, row, v, v < Hv, yv[k], gf[k], rstd, qscale, amax_unused);
         }
     }
 }

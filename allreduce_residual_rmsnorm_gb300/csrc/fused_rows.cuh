@@ -23,8 +23,7 @@
 // spin: an atomic ticket).
 #pragma once
 
-#include "ar_common.cuh"
-#include "ar_internal.h"
+#include "fused_core.cuh"
 
 namespace arf {
 
@@ -79,12 +78,10 @@ fused_rows_kernel(const FusedArgs a)
             P[r] = a.partial[r];
     }
 
-    uint4 gv[VPT];
+    float gf[VPT][8];
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-        const int v = g + k * G;
-        gv[k] = v < Hv ? ld_keep(a.gamma + (size_t)v * 16) : make_uint4(0, 0, 0, 0);
-    }
+    for (int k = 0; k < VPT; ++k)
+        load_gamma<D>(a.gamma, g + k * G, g + k * G < Hv, gf[k]);
     float qscale = 0.0f;
     if (pat & (AR_QUANT_FP8 | AR_QUANT_NVFP4))
         qscale = *a.scale_factor;
@@ -153,7 +150,7 @@ fused_rows_kernel(const FusedArgs a)
                     }
                 }
             }
-            // ---- rank sum, residual add, sum of squares
+            // ---- rank sum (fp32, rank order), residual add, sum of squares
 #pragma unroll
             for (int kk = 0; kk < KCH; ++kk) {
                 const int k = k0 + kk;
@@ -162,30 +159,13 @@ fused_rows_kernel(const FusedArgs a)
                     float s[8];
                     unpack8<D>(raw[kk][0], s);
 #pragma unroll
-                    for (int r = 1; r < RMAX; ++r) {
-                        if (r < R) {
-                            float t[8];
-                            unpack8<D>(raw[kk][r], t);
-#pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                s[i] = __fadd_rn(s[i], t[i]);
-                        }
-                    }
-                    float af[8], xf[8];
-                    unpack8<D>(pack8<D>(s), af);
-                    unpack8<D>(xr[kk], xf);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        af[i] = __fadd_rn(af[i], xf[i]);
-                    const uint4 y = pack8<D>(af);
+                    for (int r = 1; r < RMAX; ++r)
+                        if (r < R)
+                            add8<D>(s, raw[kk][r]);
+                    const uint4 y = residual_vec<D>(s, xr[kk], ss);
                     yv[k] = y;
                     if (pat & AR_RESIDUAL_OUT)
                         st_vec(a.residual_out + roff + (size_t)v * 16, y);
-                    float yf[8];
-                    unpack8<D>(y, yf);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        df_add_term(ss, __fmul_rn(yf[i], yf[i]));
                 } else {
                     yv[k] = make_uint4(0, 0, 0, 0);
                 }
@@ -198,67 +178,16 @@ fused_rows_kernel(const FusedArgs a)
             if (lane == 0)
                 red[parity][warp] = ss;
             __syncthreads();
-            DF tot = red[parity][0];
-            for (int w = 1; w < nwarps; ++w)
-                tot = df_add(tot, red[parity][w]);
-            ss = tot;
+            ss = block_combine(red[parity], nwarps, lane);
             parity ^= 1;
         }
-        const float ss32 = df_round(ss);
-        const float ms = __fdiv_rn(ss32, (float)H);
-        const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, a.eps)));
+        const float rstd = inv_rms(ss, H, a.eps);
 
         // ---- normalise, optional outputs
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int v = g + k * G;
-            const bool ok = v < Hv;
-            float yf[8], gf[8], nf[8];
-            unpack8<D>(yv[k], yf);
-            unpack8<D>(gv[k], gf);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                nf[i] = __fmul_rn(__fmul_rn(yf[i], rstd), gf[i]);
-            const uint4 nv = pack8<D>(nf);
-            if (ok && (pat & AR_NORM_OUT))
-                st_vec(a.norm_out + roff + (size_t)v * 16, nv);
-            float nq[8];
-            unpack8<D>(nv, nq);
-            if (a.amax_out && ok) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    amax_local = fmaxf(amax_local, fabsf(nq[i]));
-            }
-            if (pat & AR_QUANT_FP8) {
-                float t[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    t[i] = __fmul_rn(nq[i], qscale);
-                const uint2 c = e4m3x8(t);
-                if (ok)
-                    st_u2(a.quant_out + (size_t)row * H + (size_t)v * 8, c.x, c.y);
-            }
-            if (pat & AR_QUANT_NVFP4) {
-                float bm = 0.0f;
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    bm = fmaxf(bm, fabsf(nq[i]));
-                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
-                const uint32_t sf = e4m3_byte(__fmul_rn(qscale, __fdiv_rn(bm, 6.0f)));
-                const float dec = e4m3_to_f32(sf);
-                const float enc = dec == 0.0f ? 0.0f : __fdiv_rn(qscale, dec);
-                float t[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    t[i] = __fmul_rn(nq[i], enc);
-                const uint32_t codes = e2m1x8(t);
-                if (ok) {
-                    *reinterpret_cast<uint32_t*>(a.quant_out + (size_t)row * (H / 2) +
-                                                 (size_t)v * 4) = codes;
-                    if ((v & 1) == 0)
-                        a.scale_out[(size_t)row * (H / 16) + (v >> 1)] = (uint8_t)sf;
-                }
-            }
+            normalize_vec<D>(a, pat, row, v, v < Hv, yv[k], gf[k], rstd, qscale, amax_local);
         }
     }
 
