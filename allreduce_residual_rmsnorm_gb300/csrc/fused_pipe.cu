@@ -23,6 +23,7 @@
 #include "fused_core.cuh"
 
 #include <mutex>
+#include <stdlib.h>
 
 namespace arf {
 
@@ -52,15 +53,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
         : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+// try_wait with a suspend-time hint: a waiting warp sleeps in the barrier
+// unit (up to `hint_ns`) instead of spinning through issue slots.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t hint_ns)
 {
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(done)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
         : "memory");
     return done != 0;
 }
@@ -68,10 +71,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 // Wait for completion of the phase with parity `parity`; false after timeout_ns.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns)
 {
-    if (mbar_try_wait(bar, parity))
+    if (mbar_try_wait(bar, parity, 1000u))
         return true;
     const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_try_wait(bar, parity, 1000u)) {
         if (globaltimer_ns() - t0 > timeout_ns)
             return false;
     }
@@ -110,7 +113,7 @@ struct Ring {
 };
 
 template <class D, int VPT>
-__global__ void __launch_bounds__(544, 1)
+__global__ void __launch_bounds__(VPT == 1 ? 1024 : 544, 1)
 fused_pipe_kernel(const FusedArgs a, const int S, const int NC)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -191,10 +194,6 @@ fused_pipe_kernel(const FusedArgs a, const int S, const int NC)
 
     // ----------------------------------------------------------- consumers
     const int g = tid;
-    float gf[VPT][8];
-#pragma unroll
-    for (int k = 0; k < VPT; ++k)
-        load_gamma<D>(a.gamma, g + k * NC, g + k * NC < Hv, gf[k]);
     float qscale = 0.0f;
     if (pat & (AR_QUANT_FP8 | AR_QUANT_NVFP4))
         qscale = *a.scale_factor;
@@ -264,7 +263,9 @@ fused_pipe_kernel(const FusedArgs a, const int S, const int NC)
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int v = g + k * NC;
-            normalize_vec<D>(a, pat, row, v, v < Hv, yv[k], gf[k], rstd, qscale, amax_unused);
+            float gf[8];
+            load_gamma<D>(a.gamma, v, v < Hv, gf);   // L1-resident across rows
+            normalize_vec<D>(a, pat, row, v, v < Hv, yv[k], gf, rstd, qscale, amax_unused);
         }
     }
 }
@@ -278,7 +279,6 @@ const void* pipe_fn(int vpt)
 {
     switch (vpt) {
     case 1: return (const void*)fused_pipe_kernel<D, 1>;
-    case 2: return (const void*)fused_pipe_kernel<D, 2>;
     case 4: return (const void*)fused_pipe_kernel<D, 4>;
     case 8: return (const void*)fused_pipe_kernel<D, 8>;
     default: return nullptr;
@@ -297,7 +297,9 @@ template <class D>
 cudaError_t launch_t(const FusedArgs& a, const LaunchCfg& c)
 {
     const int Hv = a.H / 8;
-    const int vpt = pow2_at_least((Hv + 511) / 512);
+    // one 16-byte vector per consumer thread while that fits a block
+    // (<= 992 consumers + the producer warp), else <= 512 consumers
+    const int vpt = Hv <= 992 ? 1 : pow2_at_least((Hv + 511) / 512);
     const void* fn = pipe_fn<D>(vpt);
     if (!fn)
         return cudaErrorInvalidValue;
@@ -306,6 +308,11 @@ cudaError_t launch_t(const FusedArgs& a, const LaunchCfg& c)
     int S = (int)((kSmemLimit - kSmemTail) / stage_bytes);
     if (S > kMaxStages)
         S = kMaxStages;
+    if (const char* e = getenv("ARF_PIPE_STAGES")) {   // temporary sweep knob
+        const int want = atoi(e);
+        if (want >= 2 && want < S)
+            S = want;
+    }
     if (S < 2)
         return cudaErrorInvalidValue;
     const uint32_t smem = (uint32_t)S * stage_bytes + kSmemTail;

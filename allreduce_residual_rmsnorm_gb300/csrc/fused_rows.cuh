@@ -27,13 +27,18 @@
 
 namespace arf {
 
+// Block size bound: one vector per thread rows use up to 1024 threads;
+// wider rows (several vectors per thread) at most 512.
 template <class D, int RMAX, int VPT, bool WARP_ROW>
-__global__ void __launch_bounds__(WARP_ROW ? 256 : 512)
+__global__ void __launch_bounds__(WARP_ROW ? 256 : (VPT == 1 ? 1024 : 512))
 fused_rows_kernel(const FusedArgs a)
 {
-    // vectors loaded per batch: keep about 16 x 16 B of partials in flight per thread
-    constexpr int KCH = (16 / RMAX) < 1 ? 1 : ((16 / RMAX) > VPT ? VPT : (16 / RMAX));
+    // ranks loaded per batch (at most 8 x 16 B of partials in flight per vector)
+    constexpr int RB = RMAX < 8 ? RMAX : 8;
+    // vectors per batch: about 16 partial loads in flight per thread
+    constexpr int KCH = (16 / RB) > VPT ? VPT : (16 / RB);
     static_assert(VPT % KCH == 0, "batch must divide VPT");
+    static_assert(RMAX % RB == 0, "rank batch must divide RMAX");
 
     const int H = a.H;
     const int Hv = H >> 3;
@@ -78,10 +83,6 @@ fused_rows_kernel(const FusedArgs a)
             P[r] = a.partial[r];
     }
 
-    float gf[VPT][8];
-#pragma unroll
-    for (int k = 0; k < VPT; ++k)
-        load_gamma<D>(a.gamma, g + k * G, g + k * G < Hv, gf[k]);
     float qscale = 0.0f;
     if (pat & (AR_QUANT_FP8 | AR_QUANT_NVFP4))
         qscale = *a.scale_factor;
@@ -97,72 +98,88 @@ fused_rows_kernel(const FusedArgs a)
 
 #pragma unroll
         for (int k0 = 0; k0 < VPT; k0 += KCH) {
-            uint4 raw[KCH][RMAX];
+            float s[KCH][8];
             uint4 xr[KCH];
-            // ---- loads of this batch (all in flight together)
 #pragma unroll
-            for (int kk = 0; kk < KCH; ++kk) {
-                const int v = g + (k0 + kk) * G;
-                if (v < Hv) {
+            for (int r0 = 0; r0 < RMAX; r0 += RB) {
+                if (r0 >= R)
+                    break;
+                uint4 raw[KCH][RB];
+                // ---- loads of this batch (all in flight together)
 #pragma unroll
-                    for (int r = 0; r < RMAX; ++r)
-                        if (r < R)
-                            raw[kk][r] = a.lamport ? ld_poll(P[r] + roff + (size_t)v * 16)
-                                                   : ld_stream(P[r] + roff + (size_t)v * 16);
-                    xr[kk] = ld_stream(a.residual_in + roff + (size_t)v * 16);
+                for (int kk = 0; kk < KCH; ++kk) {
+                    const int v = g + (k0 + kk) * G;
+                    if (v < Hv) {
+#pragma unroll
+                        for (int rr = 0; rr < RB; ++rr)
+                            if (r0 + rr < R)
+                                raw[kk][rr] = a.lamport ? ld_poll(P[r0 + rr] + roff + (size_t)v * 16)
+                                                        : ld_stream(P[r0 + rr] + roff + (size_t)v * 16);
+                        if (r0 == 0)
+                            xr[kk] = ld_stream(a.residual_in + roff + (size_t)v * 16);
+                    }
                 }
-            }
-            // ---- Lamport: re-poll until no sentinel word is left (bounded)
-            if (a.lamport) {
-                bool pend = false;
+                // ---- Lamport: re-poll until no sentinel word is left (bounded)
+                if (a.lamport) {
+                    bool pend = false;
 #pragma unroll
-                for (int kk = 0; kk < KCH; ++kk)
+                    for (int kk = 0; kk < KCH; ++kk)
 #pragma unroll
-                    for (int r = 0; r < RMAX; ++r)
-                        if (r < R && g + (k0 + kk) * G < Hv)
-                            pend |= has_sentinel(raw[kk][r]);
-                if (pend) {
-                    const uint64_t t0 = globaltimer_ns();
-                    while (true) {
-                        pend = false;
-                        int first = -1;
+                        for (int rr = 0; rr < RB; ++rr)
+                            if (r0 + rr < R && g + (k0 + kk) * G < Hv)
+                                pend |= has_sentinel(raw[kk][rr]);
+                    if (pend) {
+                        const uint64_t t0 = globaltimer_ns();
+                        while (true) {
+                            pend = false;
+                            int first = -1;
 #pragma unroll
-                        for (int kk = 0; kk < KCH; ++kk) {
-                            const int v = g + (k0 + kk) * G;
+                            for (int kk = 0; kk < KCH; ++kk) {
+                                const int v = g + (k0 + kk) * G;
 #pragma unroll
-                            for (int r = 0; r < RMAX; ++r)
-                                if (r < R && v < Hv && has_sentinel(raw[kk][r])) {
-                                    raw[kk][r] = ld_poll(P[r] + roff + (size_t)v * 16);
-                                    if (has_sentinel(raw[kk][r])) {
-                                        pend = true;
-                                        if (first < 0)
-                                            first = r;
+                                for (int rr = 0; rr < RB; ++rr)
+                                    if (r0 + rr < R && v < Hv && has_sentinel(raw[kk][rr])) {
+                                        raw[kk][rr] = ld_poll(P[r0 + rr] + roff + (size_t)v * 16);
+                                        if (has_sentinel(raw[kk][rr])) {
+                                            pend = true;
+                                            if (first < 0)
+                                                first = r0 + rr;
+                                        }
                                     }
-                                }
+                            }
+                            if (!pend)
+                                break;
+                            if (globaltimer_ns() - t0 > a.timeout_ns) {
+                                record_error(a.state, AR_ERR_TIMEOUT, row * 32 + first);
+                                break;
+                            }
+                            __nanosleep(256);
                         }
-                        if (!pend)
-                            break;
-                        if (globaltimer_ns() - t0 > a.timeout_ns) {
-                            record_error(a.state, AR_ERR_TIMEOUT, row * 32 + first);
-                            break;
+                    }
+                }
+                // ---- fold this rank batch into the fp32 sum (rank order)
+#pragma unroll
+                for (int kk = 0; kk < KCH; ++kk) {
+                    if (g + (k0 + kk) * G < Hv) {
+#pragma unroll
+                        for (int rr = 0; rr < RB; ++rr) {
+                            if (r0 + rr < R) {
+                                if (r0 + rr == 0)
+                                    unpack8<D>(raw[kk][rr], s[kk]);
+                                else
+                                    add8<D>(s[kk], raw[kk][rr]);
+                            }
                         }
-                        __nanosleep(256);
                     }
                 }
             }
-            // ---- rank sum (fp32, rank order), residual add, sum of squares
+            // ---- residual add, sum of squares
 #pragma unroll
             for (int kk = 0; kk < KCH; ++kk) {
                 const int k = k0 + kk;
                 const int v = g + k * G;
                 if (v < Hv) {
-                    float s[8];
-                    unpack8<D>(raw[kk][0], s);
-#pragma unroll
-                    for (int r = 1; r < RMAX; ++r)
-                        if (r < R)
-                            add8<D>(s, raw[kk][r]);
-                    const uint4 y = residual_vec<D>(s, xr[kk], ss);
+                    const uint4 y = residual_vec<D>(s[kk], xr[kk], ss);
                     yv[k] = y;
                     if (pat & AR_RESIDUAL_OUT)
                         st_vec(a.residual_out + roff + (size_t)v * 16, y);
@@ -183,11 +200,13 @@ fused_rows_kernel(const FusedArgs a)
         }
         const float rstd = inv_rms(ss, H, a.eps);
 
-        // ---- normalise, optional outputs
+        // ---- normalise, optional outputs (gamma re-read per row: L1-resident)
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int v = g + k * G;
-            normalize_vec<D>(a, pat, row, v, v < Hv, yv[k], gf[k], rstd, qscale, amax_local);
+            float gf[8];
+            load_gamma<D>(a.gamma, v, v < Hv, gf);
+            normalize_vec<D>(a, pat, row, v, v < Hv, yv[k], gf, rstd, qscale, amax_local);
         }
     }
 
