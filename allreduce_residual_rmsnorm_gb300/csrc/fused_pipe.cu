@@ -279,6 +279,7 @@ const void* pipe_fn(int vpt)
 {
     switch (vpt) {
     case 1: return (const void*)fused_pipe_kernel<D, 1>;
+    case 2: return (const void*)fused_pipe_kernel<D, 2>;
     case 4: return (const void*)fused_pipe_kernel<D, 4>;
     case 8: return (const void*)fused_pipe_kernel<D, 8>;
     default: return nullptr;
