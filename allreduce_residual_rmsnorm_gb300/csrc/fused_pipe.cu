@@ -23,7 +23,6 @@
 #include "fused_core.cuh"
 
 #include <mutex>
-#include <stdlib.h>
 
 namespace arf {
 
@@ -97,6 +96,7 @@ __device__ __forceinline__ void consumer_sync(int nthreads)
 constexpr int kMaxStages = 32;
 constexpr uint32_t kSmemLimit = 232448;  // 227 KB opt-in dynamic shared memory per block
 constexpr uint32_t kSmemTail = 2048;     // barriers, reduction slots, flags
+constexpr uint32_t kRingTarget = 163840; // bytes of stages per block
 
 }  // namespace
 
@@ -113,7 +113,7 @@ struct Ring {
 };
 
 template <class D, int VPT>
-__global__ void __launch_bounds__(VPT == 1 ? 1024 : 544, 1)
+__global__ void __launch_bounds__(544, 1)
 fused_pipe_kernel(const FusedArgs a, const int S, const int NC)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -298,22 +298,24 @@ template <class D>
 cudaError_t launch_t(const FusedArgs& a, const LaunchCfg& c)
 {
     const int Hv = a.H / 8;
-    // one 16-byte vector per consumer thread while that fits a block
-    // (<= 992 consumers + the producer warp), else <= 512 consumers
-    const int vpt = Hv <= 992 ? 1 : pow2_at_least((Hv + 511) / 512);
+    // at most 512 consumer threads: more consumer warps cost more barrier
+    // arrivals per byte than they win in latency hiding (measured at H = 7168)
+    const int vpt = pow2_at_least((Hv + 511) / 512);
     const void* fn = pipe_fn<D>(vpt);
     if (!fn)
         return cudaErrorInvalidValue;
     const int NC = ((Hv + vpt - 1) / vpt + 31) / 32 * 32;
     const uint32_t stage_bytes = (uint32_t)a.H * 2;
-    int S = (int)((kSmemLimit - kSmemTail) / stage_bytes);
+    // ring depth: ~160 KB of copies in flight per SM (a sweep at H = 7168 was
+    // flat from 10 to 12 stages and lost bandwidth above 16 and below 8)
+    int S = (int)(kRingTarget / stage_bytes);
+    if (S < 4)
+        S = 4;
+    const int S_fit = (int)((kSmemLimit - kSmemTail) / stage_bytes);
+    if (S > S_fit)
+        S = S_fit;
     if (S > kMaxStages)
         S = kMaxStages;
-    if (const char* e = getenv("ARF_PIPE_STAGES")) {   // temporary sweep knob
-        const int want = atoi(e);
-        if (want >= 2 && want < S)
-            S = want;
-    }
     if (S < 2)
         return cudaErrorInvalidValue;
     const uint32_t smem = (uint32_t)S * stage_bytes + kSmemTail;
