@@ -44,6 +44,7 @@ AR_MAX_RANKS = 16
 AR_ONESHOT_MAX_TOKENS = 128
 AR_BARRIER_FLAG_COUNT = 256
 AR_MAX_HIDDEN = 32768
+AR_NOALLOC_SLOT_BYTES = 4 << 20
 
 PATTERNS = {
     "res_norm": AR_RESIDUAL_OUT | AR_NORM_OUT,
@@ -120,13 +121,15 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.ar_fusion_norm_amax.argtypes = [_vp, ctypes.POINTER(_vp), _i, _i, _i, _i, _vp, _vp,
                                       ctypes.c_float, _vp, _vp]
     L.ar_fusion_sum.argtypes = [ctypes.POINTER(_vp), _i, ctypes.c_size_t, _i, _vp, _vp]
+    L.ar_fusion_run_noalloc.argtypes = [ctypes.POINTER(_vp), _i, _i, _i, _i, _vp, _vp,
+                                        ctypes.c_float, _i, _vp, _vp, _vp, _vp, _vp, _vp]
     for name in ("ar_fusion_workspace_bytes", "ar_fusion_workspace_create",
                  "ar_fusion_workspace_destroy", "ar_fusion_workspace_info",
                  "ar_fusion_workspace_copy_state", "ar_fusion_workspace_status",
                  "ar_fusion_workspace_reset", "ar_fusion_workspace_set_timeout_ns",
                  "ar_fusion_workspace_set_variant", "ar_fusion_workspace_set_mode",
                  "ar_fusion_workspace_stage", "ar_fusion_run", "ar_fusion_norm_amax",
-                 "ar_fusion_sum"):
+                 "ar_fusion_sum", "ar_fusion_run_noalloc"):
         getattr(L, name).restype = _i
     _lib = L
     return L
@@ -311,3 +314,16 @@ def ar_fusion_sum(bufs, out: torch.Tensor, n: int | None = None, stream=None) ->
         n = out.numel()
     _check(lib().ar_fusion_sum(_ptr_array(bufs), len(bufs), n, _dtype_id(out), _ptr(out),
                                _stream(stream)))
+
+
+def ar_fusion_run_noalloc(partials, residual_in: torch.Tensor, gamma: torch.Tensor, eps: float,
+                          pattern: int, residual_out=None, norm_out=None, quant_out=None,
+                          scale_out=None, scale_factor=None, stream=None) -> None:
+    """The one-shot fused call without a workspace (no device allocation):
+    scratch lives in a fixed device array inside the library."""
+    tokens, hidden = residual_in.shape[0], residual_in.shape[-1]
+    _check(lib().ar_fusion_run_noalloc(_ptr_array(partials), len(partials), tokens, hidden,
+                                       _dtype_id(residual_in), _ptr(residual_in), _ptr(gamma),
+                                       ctypes.c_float(eps), pattern, _ptr(residual_out),
+                                       _ptr(norm_out), _ptr(quant_out), _ptr(scale_out),
+                                       _ptr(scale_factor), _stream(stream)))

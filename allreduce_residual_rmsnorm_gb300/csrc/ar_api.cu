@@ -334,6 +334,12 @@ int launch_fused(ar_fusion_ws* ws, const FusedArgs& a, cudaStream_t s)
 
 }  // namespace
 
+int arf::set_last_error(int code, const char* msg)
+{
+    g_err = msg;
+    return code;
+}
+
 // ======================================================================= ABI
 
 extern "C" {

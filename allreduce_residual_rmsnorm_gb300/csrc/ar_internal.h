@@ -48,4 +48,7 @@ struct SumArgs {
 };
 cudaError_t launch_vector_sum(int dtype, const SumArgs& a, const LaunchCfg& c);
 
+// Record `msg` as the calling thread's ar_fusion_last_error() text; returns code.
+int set_last_error(int code, const char* msg);
+
 }  // namespace arf

@@ -286,6 +286,45 @@ int ar_fusion_norm_amax(ar_fusion_ws* ws, const void* const* partials, int nrank
 int ar_fusion_sum(const void* const* bufs, int nranks, size_t n, int dtype, void* out,
                   void* stream);
 
+/* ------------------------------------------------- no-allocation call -- */
+
+/* Fixed scratch of ar_fusion_run_noalloc: three slots and the slot state,
+ * one array per GPU that loads the library, kept until the process exits. */
+#define AR_NOALLOC_SLOT_BYTES (4u << 20)
+#define AR_NOALLOC_SCRATCH_BYTES (3u * AR_NOALLOC_SLOT_BYTES + 256u)
+
+/* The one-shot fused call (same operation, arguments and results as
+ * ar_fusion_run with caller partials) for callers that must not allocate
+ * device memory: code inside a host framework that owns the whole device
+ * memory budget and forbids plugins to allocate, or code on a latency-critical
+ * path where cudaMalloc / cudaFree (which can synchronise the device) are not
+ * allowed.  The pages have no counterpart: there the workspace is always
+ * allocated (TensorRT-LLM Workspace, FlashInfer workspace creation).
+ *
+ * No workspace: the partials (host array of `nranks` device pointers, each
+ * [tokens][hidden] D) are staged by a kernel into one of three slots of a
+ * fixed device array of AR_NOALLOC_SCRATCH_BYTES, with the -0.0f sentinel
+ * flip, then read, summed, normalised and quantised by the Lamport-mode kernel,
+ * which refills the previous call's slot with the sentinel and advances the
+ * slot index -- all on `stream`.  Nothing is allocated: no cudaMalloc,
+ * cudaFree or allocating library call.
+ *
+ * Limits: nranks * tokens * hidden_dim * 2 <= AR_NOALLOC_SLOT_BYTES, else
+ * AR_ERR_CAPACITY before anything runs.  Other argument rules and errors as
+ * ar_fusion_run.
+ * Set-up: the first call on each device (the device current at the call)
+ * looks up the array's device address (cudaGetSymbolAddress) and launches a
+ * one-time fill of it on `stream`; make that first call before any stream
+ * capture.
+ * Sharing: every call on a device uses the same array and leaves the slot
+ * state for the next call; calls whose work overlaps on the GPU (different
+ * streams without ordering between them) race on it and give undefined
+ * results.  Serialise them (one stream, or events). */
+int ar_fusion_run_noalloc(const void* const* partials, int nranks, int tokens, int hidden_dim,
+                          int dtype, const void* residual_in, const void* gamma, float eps,
+                          int pattern, void* residual_out, void* norm_out, void* quant_out,
+                          void* scale_out, const float* scale_factor, void* stream);
+
 /* ---------------------------------------------------------- utilities -- */
 
 /* Message for the last failed call on this thread ("" if none). */
