@@ -244,15 +244,16 @@ __host__ __device__ __forceinline__ void df_add_term(DF& a, float t)
     a.lo = rn_add(a.lo, err);
 }
 
+// Pair addition: the high parts are added exactly (TwoSum) and every rounding
+// error lands in lo; lo is not renormalised into hi between steps (its own
+// rounding errors are ~2^-24 of an already tiny value), which keeps the
+// operation symmetric in a and b -- every lane of an xor butterfly ends with
+// the same bits.
 __host__ __device__ __forceinline__ DF df_add(DF a, DF b)
 {
     float s, err;
     two_sum(a.hi, b.hi, s, err);
-    const float lo = rn_add(rn_add(a.lo, b.lo), err);
-    // renormalise: hi + lo2 == s + lo exactly (|s| >= |lo|)
-    const float hi = rn_add(s, lo);
-    const float lo2 = rn_add(lo, -rn_add(hi, -s));
-    return DF{hi, lo2};
+    return DF{s, rn_add(rn_add(a.lo, b.lo), err)};
 }
 
 __host__ __device__ __forceinline__ float df_round(DF a)

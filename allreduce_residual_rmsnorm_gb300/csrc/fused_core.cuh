@@ -38,13 +38,41 @@ __device__ __forceinline__ float inv_rms(DF ss, int H, float eps)
     return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
 }
 
-// Combine one DF value per warp (nw <= 32 values in `slots`) in a fixed order
-// that every warp of the block reproduces bit for bit: lane l takes slot l,
-// then an xor butterfly.
-__device__ __forceinline__ DF block_combine(const DF* slots, int nw, int lane)
+// Row rstd from one DF partial per warp.  Each warp sums its lanes; warp 0
+// combines the nw warp sums (lane l takes slot l, then an xor butterfly),
+// computes rstd once and publishes it; `sync` is the barrier of the threads
+// that share the row (a __syncthreads or a named barrier).  Two slot sets
+// alternate by row parity, so one row's slots are never overwritten before
+// every thread has read them.
+struct BlockSync {
+    __device__ __forceinline__ void operator()() const { __syncthreads(); }
+};
+
+// barrier 1 over the first n threads of the block (the consumer warps)
+struct NamedSync {
+    int n;
+    __device__ __forceinline__ void operator()() const
+    {
+        asm volatile("bar.sync 1, %0;" ::"r"(n) : "memory");
+    }
+};
+
+template <class Sync>
+__device__ __forceinline__ float row_rstd(DF ss, DF* slots, float* rstd_slot, int warp, int lane,
+                                          int nw, int H, float eps, Sync sync)
 {
-    DF v = lane < nw ? slots[lane] : DF{0.0f, 0.0f};
-    return df_warp_sum(v);
+    ss = df_warp_sum(ss);
+    if (lane == 0)
+        slots[warp] = ss;
+    sync();
+    if (warp == 0) {
+        DF v = lane < nw ? slots[lane] : DF{0.0f, 0.0f};
+        v = df_warp_sum(v);
+        if (lane == 0)
+            *rstd_slot = inv_rms(v, H, eps);
+    }
+    sync();
+    return *rstd_slot;
 }
 
 // gamma of one vector as fp32 (loaded once per kernel)

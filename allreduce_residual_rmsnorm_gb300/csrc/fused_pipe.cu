@@ -88,11 +88,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         : "memory");
 }
 
-__device__ __forceinline__ void consumer_sync(int nthreads)
-{
-    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
-}
-
 constexpr int kMaxStages = 32;
 constexpr uint32_t kSmemLimit = 232448;  // 227 KB opt-in dynamic shared memory per block
 constexpr uint32_t kSmemTail = 2048;     // barriers, reduction slots, flags
@@ -125,7 +120,8 @@ fused_pipe_kernel(const FusedArgs a, const int S, const int NC)
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * stage_bytes);
     uint64_t* empty = full + kMaxStages;
     DF* red = reinterpret_cast<DF*>(empty + kMaxStages);   // [2][32]
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(red + 64);
+    float* rstd_sh = reinterpret_cast<float*>(red + 64);   // [2]
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(rstd_sh + 2);
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
@@ -251,15 +247,11 @@ fused_pipe_kernel(const FusedArgs a, const int S, const int NC)
                 }
             }
         }
-        ss = df_warp_sum(ss);
-        if (lane == 0)
-            red[parity * 32 + warp] = ss;
-        consumer_sync(NC);
+        const float rstd = row_rstd(ss, red + parity * 32, &rstd_sh[parity], warp, lane, ncw, H,
+                                    a.eps, NamedSync{NC});
+        parity ^= 1;
         if (*abort_flag)
             break;
-        ss = block_combine(red + parity * 32, ncw, lane);
-        parity ^= 1;
-        const float rstd = inv_rms(ss, H, a.eps);
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int v = g + k * NC;

@@ -27,10 +27,10 @@
 
 namespace arf {
 
-// Block size bound: one vector per thread rows use up to 1024 threads;
-// wider rows (several vectors per thread) at most 512.
+// Block size bound: one vector per thread rows use up to 896 threads (72
+// registers each); wider rows (several vectors per thread) at most 512.
 template <class D, int RMAX, int VPT, bool WARP_ROW>
-__global__ void __launch_bounds__(WARP_ROW ? 256 : (VPT == 1 ? 1024 : 512))
+__global__ void __launch_bounds__(WARP_ROW ? 256 : (VPT == 1 ? 896 : 512))
 fused_rows_kernel(const FusedArgs a)
 {
     // ranks loaded per batch (at most 8 x 16 B of partials in flight per vector)
@@ -60,16 +60,15 @@ fused_rows_kernel(const FusedArgs a)
         row_step = gridDim.x;
     }
 
-    const uint8_t* P[RMAX];
+    // rank r's row data: a caller pointer (constant-bank parameter, no
+    // register copy) or, in Lamport mode, slot + r * plane
     uint32_t flag = 0;
+    const uint8_t* slot = nullptr;
+    const size_t plane = (size_t)a.T * H * 2;
     if (a.lamport) {
         flag = *reinterpret_cast<volatile uint32_t*>(&a.state->lamport_flag);
         const uint64_t clear_elems = *reinterpret_cast<volatile uint64_t*>(&a.state->clear_size);
-        const size_t plane = (size_t)a.T * H * 2;
-        const uint8_t* slot = a.lamport_base + (size_t)(flag % 3u) * a.slot_bytes;
-#pragma unroll
-        for (int r = 0; r < RMAX; ++r)
-            P[r] = slot + (size_t)r * plane;
+        slot = a.lamport_base + (size_t)(flag % 3u) * a.slot_bytes;
         // refill the retired slot with the sentinel (clear loop of the one-shot kernel)
         uint8_t* clr = a.lamport_base + (size_t)((flag + 2u) % 3u) * a.slot_bytes;
         const uint64_t nvec = clear_elems / 8;
@@ -77,17 +76,15 @@ fused_rows_kernel(const FusedArgs a)
         const uint4 sent = make_uint4(0x80000000u, 0x80000000u, 0x80000000u, 0x80000000u);
         for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += nth)
             st_vec(clr + i * 16, sent);
-    } else {
-#pragma unroll
-        for (int r = 0; r < RMAX; ++r)
-            P[r] = a.partial[r];
     }
+#define AR_RANK_PTR(r) (a.lamport ? slot + (size_t)(r) * plane : a.partial[(r)])
 
     float qscale = 0.0f;
     if (pat & (AR_QUANT_FP8 | AR_QUANT_NVFP4))
         qscale = *a.scale_factor;
 
     __shared__ DF red[2][32];
+    __shared__ float rstd_sh[2];
     int parity = 0;
     float amax_local = 0.0f;
 
@@ -113,8 +110,8 @@ fused_rows_kernel(const FusedArgs a)
 #pragma unroll
                         for (int rr = 0; rr < RB; ++rr)
                             if (r0 + rr < R)
-                                raw[kk][rr] = a.lamport ? ld_poll(P[r0 + rr] + roff + (size_t)v * 16)
-                                                        : ld_stream(P[r0 + rr] + roff + (size_t)v * 16);
+                                raw[kk][rr] = a.lamport ? ld_poll(AR_RANK_PTR(r0 + rr) + roff + (size_t)v * 16)
+                                                        : ld_stream(AR_RANK_PTR(r0 + rr) + roff + (size_t)v * 16);
                         if (r0 == 0)
                             xr[kk] = ld_stream(a.residual_in + roff + (size_t)v * 16);
                     }
@@ -139,7 +136,7 @@ fused_rows_kernel(const FusedArgs a)
 #pragma unroll
                                 for (int rr = 0; rr < RB; ++rr)
                                     if (r0 + rr < R && v < Hv && has_sentinel(raw[kk][rr])) {
-                                        raw[kk][rr] = ld_poll(P[r0 + rr] + roff + (size_t)v * 16);
+                                        raw[kk][rr] = ld_poll(AR_RANK_PTR(r0 + rr) + roff + (size_t)v * 16);
                                         if (has_sentinel(raw[kk][rr])) {
                                             pend = true;
                                             if (first < 0)
@@ -190,15 +187,14 @@ fused_rows_kernel(const FusedArgs a)
         }
 
         // ---- sum of squares over the row
-        ss = df_warp_sum(ss);
-        if (!WARP_ROW) {
-            if (lane == 0)
-                red[parity][warp] = ss;
-            __syncthreads();
-            ss = block_combine(red[parity], nwarps, lane);
+        float rstd;
+        if (WARP_ROW) {
+            rstd = inv_rms(df_warp_sum(ss), H, a.eps);
+        } else {
+            rstd = row_rstd(ss, red[parity], &rstd_sh[parity], warp, lane, nwarps, H, a.eps,
+                            BlockSync{});
             parity ^= 1;
         }
-        const float rstd = inv_rms(ss, H, a.eps);
 
         // ---- normalise, optional outputs (gamma re-read per row: L1-resident)
 #pragma unroll
@@ -209,6 +205,8 @@ fused_rows_kernel(const FusedArgs a)
             normalize_vec<D>(a, pat, row, v, v < Hv, yv[k], gf, rstd, qscale, amax_local);
         }
     }
+
+#undef AR_RANK_PTR
 
     if (a.amax_out) {
 #pragma unroll

@@ -15,11 +15,7 @@ static const void* rows_fn_vpt(int vpt)
 {
     switch (vpt) {
     case 1: return (const void*)fused_rows_kernel<D, RMAX, 1, WARP_ROW>;
-    case 2:
-        if constexpr (!WARP_ROW)
-            return nullptr;
-        else
-            return (const void*)fused_rows_kernel<D, RMAX, 2, WARP_ROW>;
+    case 2: return (const void*)fused_rows_kernel<D, RMAX, 2, WARP_ROW>;
     case 4: return (const void*)fused_rows_kernel<D, RMAX, 4, WARP_ROW>;
     case 8:
         if constexpr (WARP_ROW)
@@ -69,8 +65,8 @@ static inline int pow2_at_least(int x)
 // Geometry:
 //   WARP_ROW: 8 warps per block, one row per warp, VPT = ceil(Hv / 32) in
 //             {1, 2, 4} (hidden <= 1024).
-//   CTA_ROW : one row per block; one vector per thread up to 1024 threads
-//             (hidden <= 8192), else VPT in {4, 8} with <= 512 threads
+//   CTA_ROW : one row per block; one vector per thread up to 896 threads
+//             (hidden <= 7168), else VPT in {2, 4, 8} with <= 512 threads
 //             (hidden <= 32768).
 // Grid: enough blocks for every row, capped at what is resident at once
 // (rows are then strided over the resident blocks).
@@ -91,8 +87,8 @@ cudaError_t launch_fused_rows_t(int variant, const FusedArgs& a, const LaunchCfg
         const int cap = c.sms * blocks_per_sm(fn, threads);
         grid = need < cap ? need : cap;
     } else {
-        // one vector per thread up to 1024 threads, else <= 512 threads
-        const int vpt = Hv <= 1024 ? 1 : pow2_at_least((Hv + 511) / 512);
+        // one vector per thread up to 896 threads, else <= 512 threads
+        const int vpt = Hv <= 896 ? 1 : pow2_at_least((Hv + 511) / 512);
         if (vpt > 8)
             return cudaErrorInvalidValue;
         fn = rows_fn<D, false>(rmax, vpt);
