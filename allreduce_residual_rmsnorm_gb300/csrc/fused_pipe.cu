@@ -326,15 +326,22 @@ cudaError_t launch_t(const FusedArgs& a, const LaunchCfg& c)
 
 }  // namespace
 
+// The ring must hold one whole row (R partial rows + the residual row): its
+// stages are released only by the row's block barrier.
 bool fused_pipe_supported(int dtype, int H, int R)
 {
     (void)dtype;
-    return H % 8 == 0 && H <= AR_MAX_HIDDEN && R >= 1 && R <= AR_MAX_RANKS;
+    if (H % 8 != 0 || H > AR_MAX_HIDDEN || R < 1 || R > AR_MAX_RANKS)
+        return false;
+    uint64_t S = (kSmemLimit - kSmemTail) / ((uint64_t)H * 2);
+    if (S > kMaxStages)
+        S = kMaxStages;
+    return S >= (uint64_t)R + 1;
 }
 
 cudaError_t launch_fused_pipe(int dtype, const FusedArgs& a, const LaunchCfg& c)
 {
-    if (a.lamport || a.amax_out)
+    if (a.lamport || a.amax_out || !fused_pipe_supported(dtype, a.H, a.R))
         return cudaErrorNotSupported;
     return dtype == AR_DT_BF16 ? launch_t<Bf16>(a, c) : launch_t<Fp16>(a, c);
 }
