@@ -168,6 +168,13 @@ __device__ __forceinline__ uint4 ld_poll(const void* p)
     return v;
 }
 
+// Ask the copy engine to bring `bytes` (multiple of 16, 16-byte aligned) of
+// global memory into L2 without waiting or using registers.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // Cached 128-bit load (gamma: read by every row).
 __device__ __forceinline__ uint4 ld_keep(const void* p)
 {

@@ -93,6 +93,18 @@ fused_rows_kernel(const FusedArgs a)
         DF ss = {0.0f, 0.0f};
         uint4 yv[VPT];
 
+        // One-row-per-block, staged or caller partials: while this row is
+        // loaded and reduced, have the copy engine pull the block's next row
+        // (R partial rows + the residual row) into L2, so that its loads start
+        // from L2 instead of exposing DRAM latency at every row boundary.
+        if (!WARP_ROW && !a.lamport && threadIdx.x < (unsigned)(R + 1)) {
+            const int nrow = row + row_step;
+            if (nrow < a.T) {
+                const uint8_t* src = (int)threadIdx.x < R ? AR_RANK_PTR(threadIdx.x) : a.residual_in;
+                prefetch_l2_bulk(src + (size_t)nrow * H * 2, (uint32_t)H * 2);
+            }
+        }
+
 #pragma unroll
         for (int k0 = 0; k0 < VPT; k0 += KCH) {
             float s[KCH][8];
