@@ -97,6 +97,8 @@ fused_rows_kernel(const FusedArgs a)
         // loaded and reduced, have the copy engine pull the block's next row
         // (R partial rows + the residual row) into L2, so that its loads start
         // from L2 instead of exposing DRAM latency at every row boundary.
+        // (Measured at R = 8, T = 8192, H = 7168: one row ahead 187.8 us, two
+        // 189.8 us, three 200.3 us, none 214.1 us.)
         if (!WARP_ROW && !a.lamport && threadIdx.x < (unsigned)(R + 1)) {
             const int nrow = row + row_step;
             if (nrow < a.T) {

@@ -88,6 +88,7 @@ cudaError_t launch_fused_rows_t(int variant, const FusedArgs& a, const LaunchCfg
         grid = need < cap ? need : cap;
     } else {
         // one vector per thread up to 896 threads, else <= 512 threads
+        // (two vectors per thread measured 208 us vs 188 us at H = 7168)
         const int vpt = Hv <= 896 ? 1 : pow2_at_least((Hv + 511) / 512);
         if (vpt > 8)
             return cudaErrorInvalidValue;
