@@ -46,6 +46,8 @@ def parse():
     p.add_argument("--tokens", type=int, default=None,
                    help="smaller token count (profiling captures); default: the full workload")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--sweep", action="store_true",
+                   help="time every target workload (one JSON line each; not the bench line)")
     p.add_argument("--profile", action="store_true",
                    help="profiling run: no soak, no end-to-end leg, no CPU baseline")
     return p.parse_args()
@@ -231,8 +233,119 @@ def config_of(w, variant):
                   "(no flush needed)", "parallelism": "replicas"}
 
 
+def aggregate(world, tokens_per_rank, steps, elapsed_ms, dist=None, device=None):
+    """Whole-job throughput: the elapsed time is the maximum over ranks (every
+    rank runs the same replica workload), value = tokens of all ranks / time.
+    Returns (tokens/s, max elapsed ms)."""
+    if dist is not None and world > 1:
+        import torch
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    return world * tokens_per_rank * steps / (elapsed_ms / 1e3), elapsed_ms
+
+
+def _median(xs):
+    xs = sorted(xs)
+    return xs[len(xs) // 2]
+
+
+def run_sweep(args):
+    """Per-workload device time of one call (median of CUDA-event timings on
+    the launching stream, L2 state as noted), algorithmic bytes, GB/s and the
+    fraction of the measured copy bandwidth."""
+    import torch
+
+    import __graft_entry__
+    from allreduce_residual_rmsnorm_gb300 import binding as B
+    from allreduce_residual_rmsnorm_gb300 import workloads as W
+    __graft_entry__.build()
+    B.load()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    peak, peak_kind = measured_peak()
+    iters = max(20, args.steps)
+
+    def timed(fn, pre=None):
+        ts = []
+        for i in range(args.warmup + iters):
+            if pre:
+                pre()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            if i >= args.warmup:
+                ts.append(a.elapsed_time(b) * 1e3)
+        return _median(ts)
+
+    for w in W.FUSED:
+        inp = W.make_fused_inputs(w)
+        P, X, G = inp.partials.to(dev), inp.residual.to(dev), inp.gamma.to(dev)
+        pat = B.PATTERNS[w.pattern]
+        out = {"res": torch.empty_like(X), "norm": torch.empty_like(X)}
+        q = sf = sc = None
+        if pat & B.AR_QUANT_FP8:
+            q = torch.empty(w.T, w.H, dtype=torch.uint8, device=dev)
+        if pat & B.AR_QUANT_NVFP4:
+            q = torch.empty(w.T, w.H // 2, dtype=torch.uint8, device=dev)
+            sf = torch.empty(w.T, w.H // 16, dtype=torch.uint8, device=dev)
+        ws = B.ar_fusion_workspace_create(w.R, w.T, w.H, B.AR_DT_BF16)
+        lam = w.T <= B.AR_ONESHOT_MAX_TOKENS
+        if pat & (B.AR_QUANT_FP8 | B.AR_QUANT_NVFP4):
+            amax = torch.empty(1, device=dev)
+            B.ar_fusion_norm_amax(ws, [P[r] for r in range(w.R)], X, G, w.eps, amax)
+            a = float(amax.item())
+            k = 448.0 if pat & B.AR_QUANT_FP8 else 2688.0
+            sc = torch.tensor([k / a if a > 0 else 1.0], device=dev)
+
+        def stage():
+            for r in range(w.R):
+                B.ar_fusion_workspace_stage(ws, r, P[r])
+
+        def call():
+            B.ar_fusion_run(ws, None, X, G, w.eps, pat, out["res"], out["norm"], q, sf, sc, stream)
+
+        if not lam:
+            stage()
+            us = timed(call)
+        else:
+            us = timed(call, pre=stage)
+        rc, _ = B.ar_fusion_workspace_status(ws)
+        outb = (w.T * w.H * 2 if pat & B.AR_NORM_OUT else 0) + \
+               (w.T * w.H if pat & B.AR_QUANT_FP8 else 0) + \
+               (w.T * w.H // 2 + w.T * w.H // 16 if pat & B.AR_QUANT_NVFP4 else 0)
+        byts = w.R * w.T * w.H * 2 + w.T * w.H * 2 * (2 if pat & B.AR_RESIDUAL_OUT else 1) + outb
+        last = B.ar_fusion_workspace_info(ws)["last_variant"]
+        print(json.dumps({"sweep": w.name, "mode": "lamport" if lam else "buffer",
+                          "variant": {1: "warp_row", 2: "cta_row", 3: "bulk_pipe"}.get(last),
+                          "us": us, "tokens_per_s": w.T / (us * 1e-6), "bytes": byts,
+                          "gbs": byts / (us * 1e-6) / 1e9, "frac_of_copy_peak": byts / (us * 1e-6) / 1e9 / peak,
+                          "l2": "inputs just staged (L2-resident)" if lam or byts < 129e6 else "inputs > L2",
+                          "status": rc}), flush=True)
+        B.ar_fusion_workspace_destroy(ws)
+        del P, X, G, out, q, sf
+        torch.cuda.empty_cache()
+
+    for sw in W.SUMS:
+        x = W.make_sum_inputs(sw).to(dev)
+        out = torch.empty(sw.N, dtype=torch.float16, device=dev)
+        bufs = [x[r] for r in range(sw.R)]
+        us = timed(lambda: B.ar_fusion_sum(bufs, out, stream=stream))
+        byts = (sw.R + 1) * sw.N * 2
+        print(json.dumps({"sweep": sw.name, "us": us, "bytes": byts, "gbs": byts / (us * 1e-6) / 1e9,
+                          "frac_of_copy_peak": byts / (us * 1e-6) / 1e9 / peak,
+                          "l2": "inputs > L2" if byts > 129e6 else "L2-resident (warm)"}), flush=True)
+        del x, out
+        torch.cuda.empty_cache()
+
+
 def main():
     args = parse()
+    if args.sweep:
+        run_sweep(args)
+        return
     from allreduce_residual_rmsnorm_gb300 import workloads as W
     w = W.NVFP4_PREFILL
     if args.tokens:
@@ -325,10 +438,7 @@ def main():
     clk = clocks.summary(t_soak, t_host1)
     clk["window"] = "untimed 0.4 s soak + the timed steps"
 
-    if pg:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
+    value, total_ms = aggregate(world, T, args.steps, total_ms, pg, dev)
 
     # ---- end to end: pinned host inputs -> device, run, outputs -> host
     e2e_steps = 0 if (args.no_e2e or args.profile) else (args.e2e_steps or max(3, min(args.steps, 10)))
@@ -362,10 +472,7 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1)
-    if pg:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_value, e2e_ms = aggregate(world, T, max(e2e_steps, 1), max(e2e_ms, 1e-9), pg, dev)
     h2d = Ph.numel() * Ph.element_size() + Xh.numel() * Xh.element_size()
     d2h = (res_h.numel() * res_h.element_size() + q_h.numel() + sf_h.numel())
 
@@ -388,7 +495,7 @@ def main():
     kname = "fused_pipe_kernel" if last == B.AR_VARIANT_BULK_PIPE else "fused_rows_kernel"
     line = {
         "metric": METRIC,
-        "value": world * T * args.steps / (total_ms / 1e3),
+        "value": value,
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -405,7 +512,7 @@ def main():
                      "peak_kind": f"{peak_kind} (hbm_gbs, copy bandwidth)",
                      "algorithmic_bytes_per_launch": bytes_alg,
                      "avg_launch_us": avg_launch_s * 1e6},
-        "e2e": ({"value": world * T * e2e_steps / (e2e_ms / 1e3), "unit": "tokens/s",
+        "e2e": ({"value": e2e_value, "unit": "tokens/s",
                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h} if e2e_steps else None),
         "gpu_launches": args.steps,
         "clocks": clk,
