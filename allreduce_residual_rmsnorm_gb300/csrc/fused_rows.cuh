@@ -28,9 +28,16 @@
 namespace arf {
 
 // Block size bound: one vector per thread rows use up to 896 threads (72
-// registers each); wider rows (several vectors per thread) at most 512.
+// registers each) with up to 8 ranks, 1024 threads (64 registers) with up to
+// 4; wider rows (several vectors per thread) at most 512.
+template <int RMAX, int VPT, bool WARP_ROW>
+constexpr int rows_max_threads()
+{
+    return WARP_ROW ? 256 : (VPT == 1 ? (RMAX <= 4 ? 1024 : 896) : 512);
+}
+
 template <class D, int RMAX, int VPT, bool WARP_ROW>
-__global__ void __launch_bounds__(WARP_ROW ? 256 : (VPT == 1 ? 896 : 512))
+__global__ void __launch_bounds__(rows_max_threads<RMAX, VPT, WARP_ROW>())
 fused_rows_kernel(const FusedArgs a)
 {
     // ranks loaded per batch (at most 8 x 16 B of partials in flight per vector)

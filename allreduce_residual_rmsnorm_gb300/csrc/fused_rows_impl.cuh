@@ -66,7 +66,8 @@ static inline int pow2_at_least(int x)
 //   WARP_ROW: 8 warps per block, one row per warp, VPT = ceil(Hv / 32) in
 //             {1, 2, 4} (hidden <= 1024).
 //   CTA_ROW : one row per block; one vector per thread up to 896 threads
-//             (hidden <= 7168), else VPT in {2, 4, 8} with <= 512 threads
+//             (hidden <= 7168; up to 1024 threads, hidden <= 8192, with at
+//             most 4 ranks), else VPT in {2, 4, 8} with <= 512 threads
 //             (hidden <= 32768).
 // Grid: enough blocks for every row, capped at what is resident at once
 // (rows are then strided over the resident blocks).
@@ -89,7 +90,8 @@ cudaError_t launch_fused_rows_t(int variant, const FusedArgs& a, const LaunchCfg
     } else {
         // one vector per thread up to 896 threads, else <= 512 threads
         // (two vectors per thread measured 208 us vs 188 us at H = 7168)
-        const int vpt = Hv <= 896 ? 1 : pow2_at_least((Hv + 511) / 512);
+        const int one_vec_max = rmax <= 4 ? 1024 : 896;
+        const int vpt = Hv <= one_vec_max ? 1 : pow2_at_least((Hv + 511) / 512);
         if (vpt > 8)
             return cudaErrorInvalidValue;
         fn = rows_fn<D, false>(rmax, vpt);

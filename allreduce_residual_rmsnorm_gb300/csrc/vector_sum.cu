@@ -137,10 +137,14 @@ static cudaError_t launch_t(const SumArgs& a, const LaunchCfg& c)
     }
     const int rmax = a.R <= 2 ? 2 : a.R <= 4 ? 4 : a.R <= 8 ? 8 : 16;
     const void* fn = sum_fn<D>(rmax);
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, 0) != cudaSuccess ||
-        per_sm < 1)
-        per_sm = 1;
+    static int cached[2][17] = {};                 // blocks per SM, per type and RMAX
+    int per_sm = cached[D::id][rmax];
+    if (per_sm == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, 0) != cudaSuccess ||
+            per_sm < 1)
+            per_sm = 1;
+        cached[D::id][rmax] = per_sm;
+    }
     const uint64_t nvec = a.n / 8;
     // two vectors per thread per step; at least one block (the tail needs it)
     uint64_t blocks = (nvec + 2 * threads - 1) / (2 * threads);

@@ -29,7 +29,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "fused AR+RMSNorm tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
-KERNEL_SOURCES = ["ar_common.cuh", "fused_pipe.cu", "fused_rows.cuh", "fused_rows_impl.cuh",
+KERNEL_SOURCES = ["ar_common.cuh", "fused_core.cuh", "fused_pipe.cu", "fused_rows.cuh", "fused_rows_impl.cuh",
                   "ar_api.cu"]
 FALLBACK_HBM_GBS = 6800.0
 
@@ -251,9 +251,9 @@ def _median(xs):
 
 
 def run_sweep(args):
-    """Per-workload device time of one call (median of CUDA-event timings on
-    the launching stream, L2 state as noted), algorithmic bytes, GB/s and the
-    fraction of the measured copy bandwidth."""
+    """Per-workload device time of one call (CUDA graphs of repeated calls,
+    CUDA events around the replays; L2 state as noted), algorithmic bytes,
+    GB/s and the fraction of the measured copy bandwidth."""
     import torch
 
     import __graft_entry__
@@ -266,18 +266,32 @@ def run_sweep(args):
     peak, peak_kind = measured_peak()
     iters = max(20, args.steps)
 
-    def timed(fn, pre=None):
+    def graph_us(body, reps=20, replays=10):
+        """Device time of one `body()`: `reps` calls captured in one CUDA graph
+        (no Python or launch overhead between them), replayed `replays` times
+        between CUDA events; median over args.warmup + a few repeats."""
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                body()                       # warm-up: fills every host-side cache
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side, capture_error_mode="thread_local"):
+            for _ in range(reps):
+                body()
+        cur = torch.cuda.current_stream(dev)
         ts = []
-        for i in range(args.warmup + iters):
-            if pre:
-                pre()
+        for i in range(max(3, args.warmup) + 5):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            fn()
-            b.record(stream)
+            a.record(cur)
+            for _ in range(replays):
+                g.replay()
+            b.record(cur)
             b.synchronize()
-            if i >= args.warmup:
-                ts.append(a.elapsed_time(b) * 1e3)
+            if i >= max(3, args.warmup):
+                ts.append(a.elapsed_time(b) * 1e3 / (reps * replays))
+        del g
         return _median(ts)
 
     for w in W.FUSED:
@@ -305,13 +319,14 @@ def run_sweep(args):
                 B.ar_fusion_workspace_stage(ws, r, P[r])
 
         def call():
-            B.ar_fusion_run(ws, None, X, G, w.eps, pat, out["res"], out["norm"], q, sf, sc, stream)
+            B.ar_fusion_run(ws, None, X, G, w.eps, pat, out["res"], out["norm"], q, sf, sc)
 
         if not lam:
             stage()
-            us = timed(call)
+            us = graph_us(call)
         else:
-            us = timed(call, pre=stage)
+            # staging stands for the peers' pushes: time stage + call, minus stage
+            us = graph_us(lambda: (stage(), call())) - graph_us(stage)
         rc, _ = B.ar_fusion_workspace_status(ws)
         outb = (w.T * w.H * 2 if pat & B.AR_NORM_OUT else 0) + \
                (w.T * w.H if pat & B.AR_QUANT_FP8 else 0) + \
@@ -332,7 +347,7 @@ def run_sweep(args):
         x = W.make_sum_inputs(sw).to(dev)
         out = torch.empty(sw.N, dtype=torch.float16, device=dev)
         bufs = [x[r] for r in range(sw.R)]
-        us = timed(lambda: B.ar_fusion_sum(bufs, out, stream=stream))
+        us = graph_us(lambda: B.ar_fusion_sum(bufs, out))
         byts = (sw.R + 1) * sw.N * 2
         print(json.dumps({"sweep": sw.name, "us": us, "bytes": byts, "gbs": byts / (us * 1e-6) / 1e9,
                           "frac_of_copy_peak": byts / (us * 1e-6) / 1e9 / peak,
