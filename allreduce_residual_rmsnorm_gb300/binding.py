@@ -115,6 +115,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.ar_fusion_workspace_set_timeout_ns.argtypes = [_vp, ctypes.c_uint64]
     L.ar_fusion_workspace_set_variant.argtypes = [_vp, _i]
     L.ar_fusion_workspace_set_mode.argtypes = [_vp, _i]
+    L.ar_fusion_workspace_set_launch.argtypes = [_vp, _i, _i]
     L.ar_fusion_workspace_stage.argtypes = [_vp, _i, _vp, _i, _i, _vp]
     L.ar_fusion_run.argtypes = [_vp, ctypes.POINTER(_vp), _i, _i, _i, _i, _vp, _vp,
                                 ctypes.c_float, _i, _vp, _vp, _vp, _vp, _vp, _vp]
@@ -128,6 +129,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                  "ar_fusion_workspace_copy_state", "ar_fusion_workspace_status",
                  "ar_fusion_workspace_reset", "ar_fusion_workspace_set_timeout_ns",
                  "ar_fusion_workspace_set_variant", "ar_fusion_workspace_set_mode",
+                 "ar_fusion_workspace_set_launch",
                  "ar_fusion_workspace_stage", "ar_fusion_run", "ar_fusion_norm_amax",
                  "ar_fusion_sum", "ar_fusion_run_noalloc"):
         getattr(L, name).restype = _i
@@ -266,6 +268,10 @@ def ar_fusion_workspace_set_variant(ws: Workspace, variant: int) -> None:
 
 def ar_fusion_workspace_set_mode(ws: Workspace, mode: int) -> None:
     _check(lib().ar_fusion_workspace_set_mode(ws.handle, int(mode)))
+
+
+def ar_fusion_workspace_set_launch(ws: Workspace, cluster_size: int = 0, pdl: int = 0) -> None:
+    _check(lib().ar_fusion_workspace_set_launch(ws.handle, int(cluster_size), int(pdl)))
 
 
 def ar_fusion_workspace_stage(ws: Workspace, rank: int, src: torch.Tensor, tokens: int | None = None,

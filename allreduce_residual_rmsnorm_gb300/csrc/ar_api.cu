@@ -43,6 +43,7 @@ struct ar_fusion_ws {
         state_off;
     int variant, mode, last_variant;
     uint64_t timeout_ns;
+    int cluster, pdl;           // launch options of the fused call (0 cluster = auto)
 };
 
 namespace {
@@ -133,6 +134,9 @@ __global__ void stage_kernel(const uint4* src, uint8_t* region, uint64_t slot_by
                              uint64_t rank_off_bytes, uint64_t nvec, int lamport,
                              const ar_fusion_state* st)
 {
+    // a fused call launched with programmatic dependent launch may be
+    // scheduled now; it still waits for this copy to complete before reading
+    pdl_trigger();
     uint8_t* dst = region + rank_off_bytes;
     if (lamport) {
         const uint32_t flag = *reinterpret_cast<const volatile uint32_t*>(&st->lamport_flag);
@@ -321,7 +325,9 @@ int pick_variant(const ar_fusion_ws* ws, const FusedArgs& a)
 
 int launch_fused(ar_fusion_ws* ws, const FusedArgs& a, cudaStream_t s)
 {
-    const LaunchCfg c{ws->sms, s};
+    LaunchCfg c{ws->sms, s};
+    c.cluster = ws->cluster > 0 ? ws->cluster : 1;
+    c.pdl = ws->pdl;
     const int variant = pick_variant(ws, a);
     ws->last_variant = variant;
     cudaError_t e = variant == AR_VARIANT_BULK_PIPE ? launch_fused_pipe(ws->dtype, a, c)
@@ -401,6 +407,8 @@ int ar_fusion_workspace_create(int tp_size, int max_token_num, int hidden_dim, i
     ws->state_off = L.state_off;
     ws->variant = AR_VARIANT_AUTO;
     ws->last_variant = AR_VARIANT_AUTO;
+    ws->cluster = 0;
+    ws->pdl = 0;
     ws->mode = AR_MODE_AUTO;
     ws->timeout_ns = 2000000000ull;
     if (ws->owned) {
@@ -528,6 +536,20 @@ int ar_fusion_workspace_set_variant(ar_fusion_ws* ws, int variant)
     if (!ws || variant < AR_VARIANT_AUTO || variant > AR_VARIANT_BULK_PIPE)
         return fail(AR_ERR_INVALID, "workspace NULL or variant %d unknown", variant);
     ws->variant = variant;
+    return AR_OK;
+}
+
+int ar_fusion_workspace_set_launch(ar_fusion_ws* ws, int cluster_size, int pdl)
+{
+    if (!ws)
+        return fail(AR_ERR_INVALID, "workspace is NULL");
+    if (cluster_size != 0 && cluster_size != 1 && cluster_size != 2 && cluster_size != 4 &&
+        cluster_size != 8)
+        return fail(AR_ERR_INVALID, "cluster_size %d is not 0 (auto), 1, 2, 4 or 8", cluster_size);
+    if (pdl != 0 && pdl != 1)
+        return fail(AR_ERR_INVALID, "pdl %d is not 0 or 1", pdl);
+    ws->cluster = cluster_size;
+    ws->pdl = pdl;
     return AR_OK;
 }
 

@@ -212,6 +212,66 @@ __device__ __forceinline__ void record_error(ar_fusion_state* st, int code, int 
         atomicExch(&st->detail, detail);
 }
 
+// ------------------------------------------------------- clusters and PDL
+
+// Thread-block cluster of this block: number of CTAs (1 when the kernel was
+// launched without clusters), this CTA's rank, the cluster index and count.
+__device__ __forceinline__ unsigned cluster_size()
+{
+    unsigned r;
+    asm("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ unsigned cluster_rank()
+{
+    unsigned r;
+    asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ unsigned cluster_id()
+{
+    unsigned r;
+    asm("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ unsigned cluster_count()
+{
+    unsigned r;
+    asm("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA of the cluster; release/acquire orders shared
+// memory writes before the barrier with reads by other CTAs after it.
+__device__ __forceinline__ void cluster_barrier()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// A float pair at the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ float2 ld_dsmem_f2(const void* local, unsigned rank)
+{
+    const uint32_t la = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(la), "r"(rank));
+    float2 v;
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(ra) : "memory");
+    return v;
+}
+
+// Programmatic dependent launch: wait until the preceding grid in the stream
+// has completed and its memory is visible (a no-op without the launch
+// attribute), and allow the next grid to be scheduled early.
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_trigger()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------- double-float accumulation
 //
 // Sum of squares as an unevaluated pair (hi, lo): every square of a 16-bit

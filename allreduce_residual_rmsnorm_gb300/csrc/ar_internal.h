@@ -32,6 +32,8 @@ struct FusedArgs {
 struct LaunchCfg {
     int sms;                    // multiprocessor count of the current device
     cudaStream_t stream;
+    int cluster = 1;            // CTAs per row (one-row-per-block kernel), 1, 2, 4 or 8
+    int pdl = 0;                // programmatic dependent launch
 };
 
 // Kernel launchers (return cudaError_t of the launch).  `variant` is a

@@ -61,11 +61,17 @@ fused_rows_kernel(const FusedArgs a)
         row = blockIdx.x * nwarps + warp;
         row_step = gridDim.x * nwarps;
     } else {
-        G = blockDim.x;
-        g = threadIdx.x;
-        row = blockIdx.x;
-        row_step = gridDim.x;
+        // one row per cluster of C CTAs (C = 1 without a cluster launch):
+        // CTA `crank` holds vectors [crank * blockDim, (crank + 1) * blockDim)
+        G = blockDim.x * cluster_size();
+        g = cluster_rank() * blockDim.x + threadIdx.x;
+        row = cluster_id();
+        row_step = cluster_count();
     }
+    const unsigned C = WARP_ROW ? 1u : cluster_size();
+
+    // inputs and the slot state may be written by the preceding grid
+    pdl_wait();
 
     // rank r's row data: a caller pointer (constant-bank parameter, no
     // register copy) or, in Lamport mode, slot + r * plane
@@ -92,6 +98,7 @@ fused_rows_kernel(const FusedArgs a)
 
     __shared__ DF red[2][32];
     __shared__ float rstd_sh[2];
+    __shared__ DF part[2];          // this CTA's row partial, read by the cluster
     int parity = 0;
     float amax_local = 0.0f;
 
@@ -108,9 +115,13 @@ fused_rows_kernel(const FusedArgs a)
         // 189.8 us, three 200.3 us, none 214.1 us.)
         if (!WARP_ROW && !a.lamport && threadIdx.x < (unsigned)(R + 1)) {
             const int nrow = row + row_step;
-            if (nrow < a.T) {
+            // this CTA's slice of the row (the whole row without a cluster)
+            const size_t off = (size_t)(g - threadIdx.x) * VPT * 16;
+            const size_t len = (size_t)blockDim.x * VPT * 16;
+            if (nrow < a.T && off < (size_t)H * 2) {
                 const uint8_t* src = (int)threadIdx.x < R ? AR_RANK_PTR(threadIdx.x) : a.residual_in;
-                prefetch_l2_bulk(src + (size_t)nrow * H * 2, (uint32_t)H * 2);
+                const size_t n = off + len <= (size_t)H * 2 ? len : (size_t)H * 2 - off;
+                prefetch_l2_bulk(src + (size_t)nrow * H * 2 + off, (uint32_t)n);
             }
         }
 
@@ -211,9 +222,33 @@ fused_rows_kernel(const FusedArgs a)
         float rstd;
         if (WARP_ROW) {
             rstd = inv_rms(df_warp_sum(ss), H, a.eps);
-        } else {
+        } else if (C == 1) {
             rstd = row_rstd(ss, red[parity], &rstd_sh[parity], warp, lane, nwarps, H, a.eps,
                             BlockSync{});
+            parity ^= 1;
+        } else {
+            // block partial -> part[parity]; after the cluster barrier every
+            // warp reads the C partials (rank order) through distributed
+            // shared memory.  Partials alternate by row parity, so one cluster
+            // barrier per row suffices (a CTA can only overwrite part[p] two
+            // rows later, after every CTA has passed the next barrier).
+            ss = df_warp_sum(ss);
+            if (lane == 0)
+                red[parity][warp] = ss;
+            __syncthreads();
+            if (warp == 0) {
+                DF v = lane < nwarps ? red[parity][lane] : DF{0.0f, 0.0f};
+                v = df_warp_sum(v);
+                if (lane == 0)
+                    part[parity] = v;
+            }
+            cluster_barrier();
+            DF t = {0.0f, 0.0f};
+            if ((unsigned)lane < C) {
+                const float2 q = ld_dsmem_f2(&part[parity], (unsigned)lane);
+                t = DF{q.x, q.y};
+            }
+            rstd = inv_rms(df_warp_sum(t), H, a.eps);
             parity ^= 1;
         }
 
@@ -228,6 +263,12 @@ fused_rows_kernel(const FusedArgs a)
     }
 
 #undef AR_RANK_PTR
+
+    // no CTA may leave while another CTA of its cluster can still read its
+    // row partial
+    if (C > 1)
+        cluster_barrier();
+    pdl_trigger();
 
     if (a.amax_out) {
 #pragma unroll

@@ -54,6 +54,33 @@ static inline int blocks_per_sm(const void* fn, int threads)
     return n;
 }
 
+// clusters of C CTAs that can be resident at once (cached)
+static inline int max_clusters(const void* fn, int threads, int C)
+{
+    static std::mutex mu;
+    static std::map<std::pair<const void*, int>, int> cache;
+    std::lock_guard<std::mutex> lk(mu);
+    auto key = std::make_pair(fn, threads * 16 + C);
+    auto it = cache.find(key);
+    if (it != cache.end())
+        return it->second;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = C;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.gridDim = dim3(C);
+    cfg.blockDim = dim3(threads);
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess || n < 1)
+        n = 1;
+    cache[key] = n;
+    return n;
+}
+
 static inline int pow2_at_least(int x)
 {
     int p = 1;
@@ -69,8 +96,11 @@ static inline int pow2_at_least(int x)
 //             (hidden <= 7168; up to 1024 threads, hidden <= 8192, with at
 //             most 4 ranks), else VPT in {2, 4, 8} with <= 512 threads
 //             (hidden <= 32768).
-// Grid: enough blocks for every row, capped at what is resident at once
-// (rows are then strided over the resident blocks).
+//             With LaunchCfg::cluster = C > 1, one row per cluster of C CTAs
+//             (one vector per thread, the row's sum of squares combined through
+//             distributed shared memory) for token counts below the SM count.
+// Grid: enough blocks (clusters) for every row, capped at what is resident at
+// once (rows are then strided over the resident blocks).
 template <class D>
 cudaError_t launch_fused_rows_t(int variant, const FusedArgs& a, const LaunchCfg& c)
 {
@@ -78,6 +108,7 @@ cudaError_t launch_fused_rows_t(int variant, const FusedArgs& a, const LaunchCfg
     const int rmax = a.R <= 2 ? 2 : a.R <= 4 ? 4 : a.R <= 8 ? 8 : 16;
     const void* fn;
     int threads, grid;
+    int C = variant == AR_VARIANT_WARP_ROW ? 1 : c.cluster;
     if (variant == AR_VARIANT_WARP_ROW) {
         const int vpt = pow2_at_least((Hv + 31) / 32);
         if (vpt > 4)
@@ -91,20 +122,51 @@ cudaError_t launch_fused_rows_t(int variant, const FusedArgs& a, const LaunchCfg
         // one vector per thread up to 896 threads, else <= 512 threads
         // (two vectors per thread measured 208 us vs 188 us at H = 7168)
         const int one_vec_max = rmax <= 4 ? 1024 : 896;
-        const int vpt = Hv <= one_vec_max ? 1 : pow2_at_least((Hv + 511) / 512);
+        // a row split over a cluster of C CTAs: one vector per thread only
+        if (C > 1 && (Hv + C - 1) / C > one_vec_max)
+            C = 1;
+        const int vpt = (Hv + C - 1) / C <= one_vec_max ? 1 : pow2_at_least((Hv + 511) / 512);
         if (vpt > 8)
             return cudaErrorInvalidValue;
         fn = rows_fn<D, false>(rmax, vpt);
-        threads = ((Hv + vpt - 1) / vpt + 31) / 32 * 32;
-        const int cap = c.sms * blocks_per_sm(fn, threads);
-        grid = a.T < cap ? a.T : cap;
+        threads = ((Hv + C * vpt - 1) / (C * vpt) + 31) / 32 * 32;
+        if (C == 1) {
+            const int cap = c.sms * blocks_per_sm(fn, threads);
+            grid = a.T < cap ? a.T : cap;
+        } else {
+            int ncl = max_clusters(fn, threads, C);
+            if (ncl < 1)
+                ncl = 1;
+            grid = (a.T < ncl ? a.T : ncl) * C;
+        }
     }
     if (!fn)
         return cudaErrorInvalidValue;
     if (grid < 1)
         grid = 1;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = c.stream;
+    if (C > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = C;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (c.pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
     void* args[] = {const_cast<FusedArgs*>(&a)};
-    return cudaLaunchKernel(fn, dim3(grid), dim3(threads), args, 0, c.stream);
+    return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 }  // namespace arf

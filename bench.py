@@ -294,6 +294,21 @@ def run_sweep(args):
         del g
         return _median(ts)
 
+    def report(w, pat, ws, lam, us, cl, pdl):
+        rc, _ = B.ar_fusion_workspace_status(ws)
+        outb = (w.T * w.H * 2 if pat & B.AR_NORM_OUT else 0) + \
+               (w.T * w.H if pat & B.AR_QUANT_FP8 else 0) + \
+               (w.T * w.H // 2 + w.T * w.H // 16 if pat & B.AR_QUANT_NVFP4 else 0)
+        byts = w.R * w.T * w.H * 2 + w.T * w.H * 2 * (2 if pat & B.AR_RESIDUAL_OUT else 1) + outb
+        last = B.ar_fusion_workspace_info(ws)["last_variant"]
+        print(json.dumps({"sweep": w.name, "mode": "lamport" if lam else "buffer",
+                          "variant": {1: "warp_row", 2: "cta_row", 3: "bulk_pipe"}.get(last),
+                          "cluster": cl, "pdl": pdl,
+                          "us": us, "tokens_per_s": w.T / (us * 1e-6), "bytes": byts,
+                          "gbs": byts / (us * 1e-6) / 1e9, "frac_of_copy_peak": byts / (us * 1e-6) / 1e9 / peak,
+                          "l2": "inputs just staged (L2-resident)" if lam or byts < 129e6 else "inputs > L2",
+                          "status": rc}), flush=True)
+
     for w in W.FUSED:
         inp = W.make_fused_inputs(w)
         P, X, G = inp.partials.to(dev), inp.residual.to(dev), inp.gamma.to(dev)
@@ -321,24 +336,20 @@ def run_sweep(args):
         def call():
             B.ar_fusion_run(ws, None, X, G, w.eps, pat, out["res"], out["norm"], q, sf, sc)
 
-        if not lam:
-            stage()
-            us = graph_us(call)
-        else:
-            # staging stands for the peers' pushes: time stage + call, minus stage
-            us = graph_us(lambda: (stage(), call())) - graph_us(stage)
-        rc, _ = B.ar_fusion_workspace_status(ws)
-        outb = (w.T * w.H * 2 if pat & B.AR_NORM_OUT else 0) + \
-               (w.T * w.H if pat & B.AR_QUANT_FP8 else 0) + \
-               (w.T * w.H // 2 + w.T * w.H // 16 if pat & B.AR_QUANT_NVFP4 else 0)
-        byts = w.R * w.T * w.H * 2 + w.T * w.H * 2 * (2 if pat & B.AR_RESIDUAL_OUT else 1) + outb
-        last = B.ar_fusion_workspace_info(ws)["last_variant"]
-        print(json.dumps({"sweep": w.name, "mode": "lamport" if lam else "buffer",
-                          "variant": {1: "warp_row", 2: "cta_row", 3: "bulk_pipe"}.get(last),
-                          "us": us, "tokens_per_s": w.T / (us * 1e-6), "bytes": byts,
-                          "gbs": byts / (us * 1e-6) / 1e9, "frac_of_copy_peak": byts / (us * 1e-6) / 1e9 / peak,
-                          "l2": "inputs just staged (L2-resident)" if lam or byts < 129e6 else "inputs > L2",
-                          "status": rc}), flush=True)
+        # launch options: (cluster CTAs per row, programmatic dependent launch);
+        # decode-sized token counts also try cluster-split rows and PDL
+        opts = [(0, 0)]
+        if w.T < 152 and w.H > 1024:
+            opts += [(1, 1), (2, 0), (2, 1), (4, 1), (8, 1)]
+        for cl, pdl in opts:
+            B.ar_fusion_workspace_set_launch(ws, cl, pdl)
+            if not lam:
+                stage()
+                us = graph_us(call)
+            else:
+                # staging stands for the peers' pushes: time stage + call, minus stage
+                us = graph_us(lambda: (stage(), call())) - graph_us(stage)
+            report(w, pat, ws, lam, us, cl, pdl)
         B.ar_fusion_workspace_destroy(ws)
         del P, X, G, out, q, sf
         torch.cuda.empty_cache()

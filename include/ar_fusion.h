@@ -211,6 +211,18 @@ int ar_fusion_workspace_set_timeout_ns(ar_fusion_ws* ws, uint64_t ns);
 int ar_fusion_workspace_set_variant(ar_fusion_ws* ws, int variant);
 int ar_fusion_workspace_set_mode(ar_fusion_ws* ws, int mode);
 
+/* Launch options of later fused calls on this workspace (host-side; no CUDA
+ * call).  cluster_size: CTAs per token row for the one-row-per-block kernel
+ * (TensorRT-LLM allReduceFusionKernels.cu, allreduce_fusion_kernel_launcher
+ * splits a token over a thread-block cluster and combines the sum of squares
+ * through distributed shared memory, rms_norm): 0 = automatic, 1 = no
+ * cluster, 2, 4 or 8; used only where a row still has at least one 16-byte
+ * vector per thread.  pdl: 1 = programmatic dependent launch (the same
+ * launcher's programmaticStreamSerialization attribute): the fused kernel
+ * may be scheduled while the preceding kernel on the stream finishes and
+ * waits on the device for its results.  Errors: AR_ERR_INVALID. */
+int ar_fusion_workspace_set_launch(ar_fusion_ws* ws, int cluster_size, int pdl);
+
 /* Stage rank `rank`'s partial [tokens][hidden] (device pointer `src`) into the
  * workspace, standing in for the one-shot push of
  * allreduce_fusion_kernel_oneshot_lamport (on one GPU nothing is pushed over

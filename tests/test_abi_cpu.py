@@ -90,6 +90,7 @@ def test_run_and_calls_reject_null_workspace(L):
     assert L.ar_fusion_workspace_reset(None, None) == B.AR_ERR_INVALID
     assert L.ar_fusion_workspace_set_variant(None, 1) == B.AR_ERR_INVALID
     assert L.ar_fusion_workspace_set_mode(None, 1) == B.AR_ERR_INVALID
+    assert L.ar_fusion_workspace_set_launch(None, 2, 1) == B.AR_ERR_INVALID
     assert L.ar_fusion_workspace_set_timeout_ns(None, 5) == B.AR_ERR_INVALID
     assert L.ar_fusion_workspace_destroy(None) == B.AR_OK
 

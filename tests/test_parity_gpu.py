@@ -22,11 +22,12 @@ def make_ws(w, max_tokens=None, mem=False):
 
 
 def run_and_check(w, variant=B.AR_VARIANT_AUTO, staged=False, mode=B.AR_MODE_AUTO, inp=None,
-                  max_tokens=None):
+                  max_tokens=None, cluster=0, pdl=0):
     inp = inp or W.make_fused_inputs(w)
     ws = make_ws(w, max_tokens)
     B.ar_fusion_workspace_set_variant(ws, variant)
     B.ar_fusion_workspace_set_mode(ws, mode)
+    B.ar_fusion_workspace_set_launch(ws, cluster, pdl)
     lam = staged and (mode == B.AR_MODE_LAMPORT or
                       (mode == B.AR_MODE_AUTO and w.T <= B.AR_ONESHOT_MAX_TOKENS))
     exp = PY.oracle_expected(w, inp, lamport_flip=lam)
@@ -97,6 +98,53 @@ def test_edge_shapes(R, T, H, dtype, pattern, variant):
     stats, _, _ = run_and_check(w, variant)
     assert stats.get("residual_mismatch", 0) == 0, stats
     assert stats.get("norm_mismatch", 0) <= max(1, T * H // 100000), stats
+
+
+# ------------------------------------------- cluster-split rows, PDL launch
+
+CLUSTER_CASES = [
+    # (R, T, H, dtype, pattern)
+    W.DECODE,                                                               # 8 x 128 x 4096
+    W.FusedWorkload("cl_nvfp4", R=8, T=40, H=7168, pattern=W.RES_NORM_NVFP4, heavy_frac=0.01),
+    W.FusedWorkload("cl_fp8", R=3, T=7, H=2064, pattern=W.RES_NORM_FP8, dtype="fp16", seed=3),
+    W.FusedWorkload("cl_r16", R=16, T=5, H=8192, pattern=W.NORM, seed=4),
+]
+
+
+@pytest.mark.parametrize("w", CLUSTER_CASES, ids=lambda w: w.name)
+@pytest.mark.parametrize("cluster", [2, 4, 8])
+@pytest.mark.parametrize("staged,pdl", [(False, 0), (True, 1)])
+def test_cluster_split_rows(w, cluster, staged, pdl):
+    stats, _, _ = run_and_check(w, B.AR_VARIANT_CTA_ROW, staged, cluster=cluster, pdl=pdl)
+    assert stats.get("residual_mismatch", 0) == 0, stats
+    assert stats.get("norm_mismatch", 0) <= max(1, w.T * w.H // 100000), stats
+
+
+def test_cluster_lamport_sequence_with_pdl():
+    # several one-shot calls in a row with both launch options on: the slot
+    # state machine and the retired-slot clear still hold
+    w = W.DECODE.with_(T=48)
+    ws = make_ws(w)
+    B.ar_fusion_workspace_set_launch(ws, 4, 1)
+    for k in range(5):
+        wk = w.with_(seed=50 + k)
+        inp = W.make_fused_inputs(wk)
+        exp = PY.oracle_expected(wk, inp, lamport_flip=True)
+        got = PY.run_gpu(ws, wk, inp, staged=True)
+        PY.check_all(wk, got, exp)
+        assert np.array_equal(got["residual"], exp["residual"])
+        st = B.ar_fusion_workspace_copy_state(ws)
+        assert st["lamport_flag"] == (k + 1) % 3 and st["status"] == 0 and st["counter"] == 0
+    B.ar_fusion_workspace_destroy(ws)
+
+
+def test_set_launch_rejects_bad_values():
+    ws = make_ws(W.TINY)
+    for cl, pdl in ((3, 0), (16, 0), (-1, 0), (2, 2)):
+        with pytest.raises(B.ArFusionError) as e:
+            B.ar_fusion_workspace_set_launch(ws, cl, pdl)
+        assert e.value.code == B.AR_ERR_INVALID
+    B.ar_fusion_workspace_destroy(ws)
 
 
 @pytest.mark.parametrize("staged", [False, True])
