@@ -221,11 +221,31 @@ void oracle_lamport_flip(uint32_t* words, int64_t n_words)
 
 /* ------------------------------------------------------ fused epilogue --- */
 
+/* Sum over ranks of one element, p[r * stride] for r < R ([TRT] allreduce_sum):
+ *   acc = 0: fp32, rank order, rounded to D once by the caller (Fp32Acc, the
+ *            default of [TRT] use_fp32_acc);
+ *   acc = 1: every partial sum rounded to D (the other branch: chained add128
+ *            in the element type; [MSC] vectorSum's half-precision adds).
+ * An fp32 addition of two 16-bit values followed by one rounding to D is the
+ * correctly rounded D addition.  Returns the fp32 value before the caller's
+ * final rounding to D. */
+static float rank_sum(int dtype, int acc, const uint16_t* p, int64_t stride, int R)
+{
+    float s = dec_d(dtype, p[0]);
+    for (int r = 1; r < R; ++r) {
+        s = s + dec_d(dtype, p[(int64_t)r * stride]);
+        if (acc)
+            s = dec_d(dtype, rnd_d(dtype, s));
+    }
+    return s;
+}
+
 /*
  * For rows t in [row_begin, row_end) of a [T][H] problem:
  *
  *   s_h   = f(P[0][t][h]) + f(P[1][t][h]) + ... + f(P[R-1][t][h])
- *           fp32, rank order                        ([TRT] allreduce_sum, Fp32Acc)
+ *           fp32, rank order                        ([TRT] allreduce_sum, Fp32Acc;
+ *           acc = 1: rounded to D after every addition, see rank_sum)
  *   a_h   = rnd_D(s_h)                              (same, final cast)
  *   y_h   = rnd_D(f(a_h) + f(X[t][h]))  -> residual_out     ([TRT] add128, fused_op)
  *   ss    = sum_h f(y_h)^2   accumulated in fp64, rounded once to fp32
@@ -238,7 +258,7 @@ void oracle_lamport_flip(uint32_t* words, int64_t n_words)
  * residual_out / norm_out may be NULL (not written).  rstd_out (may be NULL)
  * receives the per-row fp32 rstd.
  */
-void oracle_fused_rows(int dtype, int R, int64_t T, int64_t H, int64_t rank_stride,
+void oracle_fused_rows(int dtype, int acc, int R, int64_t T, int64_t H, int64_t rank_stride,
                        const uint16_t* partials, const uint16_t* residual_in,
                        const uint16_t* gamma, float eps, int64_t row_begin, int64_t row_end,
                        uint16_t* residual_out, uint16_t* norm_out, float* rstd_out)
@@ -248,9 +268,7 @@ void oracle_fused_rows(int dtype, int R, int64_t T, int64_t H, int64_t rank_stri
         double ss = 0.0;
         /* pass 1: sum over ranks, round, residual add, round, square-sum */
         for (int64_t h = 0; h < H; ++h) {
-            float s = dec_d(dtype, partials[0 * rank_stride + t * H + h]);
-            for (int r = 1; r < R; ++r)
-                s = s + dec_d(dtype, partials[(int64_t)r * rank_stride + t * H + h]);
+            float s = rank_sum(dtype, acc, partials + t * H + h, rank_stride, R);
             uint16_t a = rnd_d(dtype, s);
             uint16_t y = rnd_d(dtype, dec_d(dtype, a) + dec_d(dtype, residual_in[t * H + h]));
             if (residual_out)
@@ -268,9 +286,7 @@ void oracle_fused_rows(int dtype, int R, int64_t T, int64_t H, int64_t rank_stri
             continue;
         /* pass 2: normalise (recomputes y; identical arithmetic) */
         for (int64_t h = 0; h < H; ++h) {
-            float s = dec_d(dtype, partials[0 * rank_stride + t * H + h]);
-            for (int r = 1; r < R; ++r)
-                s = s + dec_d(dtype, partials[(int64_t)r * rank_stride + t * H + h]);
+            float s = rank_sum(dtype, acc, partials + t * H + h, rank_stride, R);
             uint16_t a = rnd_d(dtype, s);
             uint16_t y = rnd_d(dtype, dec_d(dtype, a) + dec_d(dtype, residual_in[t * H + h]));
             float ny = dec_d(dtype, y) * rstd;
@@ -356,17 +372,14 @@ void oracle_quant_nvfp4(int dtype, const uint16_t* n_in, int64_t T, int64_t H, f
 
 /* out_i = rnd_D(f(in_0[i]) + f(in_1[i]) + ... + f(in_{R-1}[i])), fp32, rank
  * order ([MSC] vectorSum applied R-1 times, accumulating in fp32 as the fused
- * path does).  Element (r, i) at in[r * rank_stride + i]. */
-void oracle_sum(int dtype, int R, int64_t n, int64_t rank_stride, const uint16_t* in,
+ * path does); acc = 1: every addition rounded to D, as vectorSum's
+ * element-type adds.  Element (r, i) at in[r * rank_stride + i]. */
+void oracle_sum(int dtype, int acc, int R, int64_t n, int64_t rank_stride, const uint16_t* in,
                 uint16_t* out, int64_t i_begin, int64_t i_end)
 {
     (void)n;
-    for (int64_t i = i_begin; i < i_end; ++i) {
-        float s = dec_d(dtype, in[i]);
-        for (int r = 1; r < R; ++r)
-            s = s + dec_d(dtype, in[(int64_t)r * rank_stride + i]);
-        out[i] = rnd_d(dtype, s);
-    }
+    for (int64_t i = i_begin; i < i_end; ++i)
+        out[i] = rnd_d(dtype, rank_sum(dtype, acc, in + i, rank_stride, R));
 }
 
 /* ------------------------------------------------ workspace arithmetic --- */

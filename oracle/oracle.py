@@ -78,7 +78,7 @@ def load_library(path: str) -> ctypes.CDLL:
     L.oracle_lamport_flip.argtypes = [_u32p, ctypes.c_int64]
     L.oracle_lamport_flip.restype = None
     L.oracle_fused_rows.argtypes = [
-        ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
         _u16p, _u16p, _u16p, ctypes.c_float, ctypes.c_int64, ctypes.c_int64,
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
     L.oracle_fused_rows.restype = None
@@ -93,8 +93,8 @@ def load_library(path: str) -> ctypes.CDLL:
     L.oracle_quant_nvfp4.argtypes = [ctypes.c_int, _u16p, ctypes.c_int64, ctypes.c_int64,
                                      ctypes.c_float, _u8p, _u8p]
     L.oracle_quant_nvfp4.restype = None
-    L.oracle_sum.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
-                             _u16p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64]
+    L.oracle_sum.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
+                             ctypes.c_int64, _u16p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64]
     L.oracle_sum.restype = None
     L.oracle_workspace_sizes.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
                                          ctypes.c_int, ctypes.c_int64, ctypes.c_int64, _i64p]
@@ -176,11 +176,14 @@ def lamport_flip(bits16: np.ndarray) -> np.ndarray:
 
 
 def fused(dtype: int, partials: np.ndarray, residual_in: np.ndarray, gamma: np.ndarray,
-          eps: float, rows=None, want_residual=True, want_norm=True, threads: int | None = None):
+          eps: float, rows=None, want_residual=True, want_norm=True, threads: int | None = None,
+          acc: int = 0):
     """Residual add + RMSNorm of the rank sum.
 
     partials: uint16 [R, T, H]; residual_in: uint16 [T, H]; gamma: uint16 [H].
     ``rows``: optional (begin, end) row range; outputs cover only those rows.
+    ``acc``: 0 = fp32 rank sum rounded once; 1 = rounded to the element type
+    after every addition.
     Returns (residual_out uint16 [n, H] | None, norm_out uint16 [n, H] | None,
     rstd float32 [n]).
     """
@@ -197,7 +200,7 @@ def fused(dtype: int, partials: np.ndarray, residual_in: np.ndarray, gamma: np.n
     L = lib()
 
     def run(rb, re_):
-        L.oracle_fused_rows(dtype, R, T, H, T * H, partials, residual_in, gamma,
+        L.oracle_fused_rows(dtype, acc, R, T, H, T * H, partials, residual_in, gamma,
                             ctypes.c_float(eps), rb, re_,
                             res.ctypes.data if res is not None else None,
                             nrm.ctypes.data if nrm is not None else None,
@@ -247,15 +250,16 @@ def quant_nvfp4(dtype: int, n_bits: np.ndarray, gs: float):
     return q, s
 
 
-def vector_sum(dtype: int, ins: np.ndarray, threads: int | None = None) -> np.ndarray:
-    """ins: uint16 [R, N] -> uint16 [N], fp32 rank-order sum rounded once."""
+def vector_sum(dtype: int, ins: np.ndarray, threads: int | None = None, acc: int = 0) -> np.ndarray:
+    """ins: uint16 [R, N] -> uint16 [N], fp32 rank-order sum rounded once
+    (acc = 1: rounded to the element type after every addition)."""
     ins = np.ascontiguousarray(ins, dtype=np.uint16)
     R, N = ins.shape
     out = np.zeros(N, np.uint16)
     L = lib()
     nt = threads or host_threads()
     spans = _chunks(N, nt * 4)
-    run = lambda s: L.oracle_sum(dtype, R, N, N, ins, out.ctypes.data, s[0], s[1])  # noqa: E731
+    run = lambda s: L.oracle_sum(dtype, acc, R, N, N, ins, out.ctypes.data, s[0], s[1])  # noqa: E731
     if nt > 1 and len(spans) > 1:
         with ThreadPoolExecutor(nt) as ex:
             list(ex.map(run, spans))

@@ -40,8 +40,8 @@ def ulp_diff_bf16(a_bits, b_bits):
     return np.abs(key(a_bits) - key(b_bits))
 
 
-def run(partials, residual, gamma, eps, dtype=BF16):
-    return oracle.fused(dtype, bits(partials), bits(residual), bits(gamma), eps, threads=2)
+def run(partials, residual, gamma, eps, dtype=BF16, acc=0):
+    return oracle.fused(dtype, bits(partials), bits(residual), bits(gamma), eps, threads=2, acc=acc)
 
 
 # -------------------------------------------------- residual path (steps 1-2)
@@ -120,6 +120,50 @@ def test_rank_sum_is_rounded_before_residual_add_worked_value():
     gamma = bf(np.ones(8))
     out, _, _ = run(P, res, gamma, 1e-6)
     assert np.array_equal(out, bits(bf(np.ones((1, 8)))))
+
+
+# ------------------------------------- element-type accumulation (variant)
+
+def test_element_type_accumulation_worked_value():
+    # Partials 1, 2^-8, 2^-8.  fp32 accumulation: 1 + 2^-8 + 2^-8 = 1 + 2^-7
+    # exactly, one rounding keeps it.  bf16 accumulation: 1 + 2^-8 is a tie
+    # between bf16 neighbours 1 and 1 + 2^-7 and rounds to even (1), twice.
+    P = torch.zeros(3, 1, 8, dtype=torch.bfloat16)
+    P[0] = bf(1.0)
+    P[1] = bf(2.0 ** -8)
+    P[2] = bf(2.0 ** -8)
+    res = torch.zeros(1, 8, dtype=torch.bfloat16)
+    gamma = bf(np.ones(8))
+    out32, _, _ = run(P, res, gamma, 1e-6, acc=0)
+    out16, _, _ = run(P, res, gamma, 1e-6, acc=1)
+    assert np.all(out32 == bits(bf(1.0 + 2.0 ** -7)).item())
+    assert np.all(out16 == bits(bf(1.0)).item())
+
+
+@pytest.mark.parametrize("dtype", [BF16, FP16])
+def test_element_type_accumulation_is_chained_library_adds(dtype):
+    # torch CPU adds of two bf16 / fp16 tensors round once per addition: the
+    # chained sum p0 + p1 + ... is the element-type accumulation
+    tdt = torch.bfloat16 if dtype == BF16 else torch.float16
+    g = torch.Generator().manual_seed(31)
+    R, T, H = 6, 4, 256
+    P = torch.randn(R, T, H, generator=g).to(tdt)
+    res = torch.randn(T, H, generator=g).to(tdt)
+    gamma = (1 + 0.1 * torch.randn(H, generator=g)).to(tdt)
+    a = P[0].clone()
+    for r in range(1, R):
+        a = a + P[r]
+    out, _, _ = run(P, res, gamma, 1e-6, dtype, acc=1)
+    assert np.array_equal(out, bits(a + res))
+
+
+def test_vector_sum_element_type_accumulation():
+    g = torch.Generator().manual_seed(2)
+    x = (torch.rand(8, 5003, generator=g) * 2 - 1).to(torch.float16)
+    a = x[0].clone()
+    for r in range(1, 8):
+        a = a + x[r]
+    assert np.array_equal(oracle.vector_sum(FP16, bits(x), threads=2, acc=1), bits(a))
 
 
 # ----------------------------------------------------- RMSNorm (steps 3-5)

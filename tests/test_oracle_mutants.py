@@ -20,14 +20,15 @@ SRC = os.path.join(os.path.dirname(OM.__file__), "ar_oracle.c")
 MUTANTS = {
     "drop_residual": ("dec_d(dtype, a) + dec_d(dtype, residual_in[t * H + h]));\n            if (residual_out)",
                       "dec_d(dtype, a) + 0.0f);\n            if (residual_out)"),
-    "skip_last_rank": ("for (int r = 1; r < R; ++r)\n                s = s + dec_d(dtype, partials[(int64_t)r * rank_stride + t * H + h]);\n            uint16_t a = rnd_d(dtype, s);\n            uint16_t y = rnd_d(dtype, dec_d(dtype, a) + dec_d(dtype, residual_in[t * H + h]));\n            if (residual_out)",
-                       "for (int r = 1; r < R - 1; ++r)\n                s = s + dec_d(dtype, partials[(int64_t)r * rank_stride + t * H + h]);\n            uint16_t a = rnd_d(dtype, s);\n            uint16_t y = rnd_d(dtype, dec_d(dtype, a) + dec_d(dtype, residual_in[t * H + h]));\n            if (residual_out)"),
-    "subtract_rank": ("s = s + dec_d(dtype, partials[(int64_t)r * rank_stride + t * H + h]);\n            uint16_t a = rnd_d(dtype, s);\n            uint16_t y = rnd_d(dtype, dec_d(dtype, a) + dec_d(dtype, residual_in[t * H + h]));\n            if (residual_out)",
-                      "s = s - dec_d(dtype, partials[(int64_t)r * rank_stride + t * H + h]);\n            uint16_t a = rnd_d(dtype, s);\n            uint16_t y = rnd_d(dtype, dec_d(dtype, a) + dec_d(dtype, residual_in[t * H + h]));\n            if (residual_out)"),
+    "skip_last_rank": ("for (int r = 1; r < R; ++r) {\n        s = s + dec_d(dtype, p[(int64_t)r * stride]);",
+                       "for (int r = 1; r < R - 1; ++r) {\n        s = s + dec_d(dtype, p[(int64_t)r * stride]);"),
+    "subtract_rank": ("s = s + dec_d(dtype, p[(int64_t)r * stride]);", "s = s - dec_d(dtype, p[(int64_t)r * stride]);"),
     "no_sum_rounding": ("uint16_t y = rnd_d(dtype, dec_d(dtype, a) + dec_d(dtype, residual_in[t * H + h]));\n            if (residual_out)",
                         "uint16_t y = rnd_d(dtype, s + dec_d(dtype, residual_in[t * H + h])); (void)a;\n            if (residual_out)"),
-    "fp64_rank_sum": ("float s = dec_d(dtype, partials[0 * rank_stride + t * H + h]);\n            for (int r = 1; r < R; ++r)\n                s = s + dec_d(dtype, partials[(int64_t)r * rank_stride + t * H + h]);\n            uint16_t a = rnd_d(dtype, s);\n            uint16_t y = rnd_d(dtype, dec_d(dtype, a) + dec_d(dtype, residual_in[t * H + h]));\n            if (residual_out)",
-                      "double sd = dec_d(dtype, partials[0 * rank_stride + t * H + h]);\n            for (int r = 1; r < R; ++r)\n                sd = sd + dec_d(dtype, partials[(int64_t)r * rank_stride + t * H + h]);\n            float s = (float)sd;\n            uint16_t a = rnd_d(dtype, s);\n            uint16_t y = rnd_d(dtype, dec_d(dtype, a) + dec_d(dtype, residual_in[t * H + h]));\n            if (residual_out)"),
+    "fp64_rank_sum": ("    float s = dec_d(dtype, p[0]);\n    for (int r = 1; r < R; ++r) {\n        s = s + dec_d(dtype, p[(int64_t)r * stride]);\n        if (acc)\n            s = dec_d(dtype, rnd_d(dtype, s));\n    }\n    return s;",
+                      "    double s = dec_d(dtype, p[0]);\n    for (int r = 1; r < R; ++r) {\n        s = s + dec_d(dtype, p[(int64_t)r * stride]);\n        if (acc)\n            s = dec_d(dtype, rnd_d(dtype, (float)s));\n    }\n    return (float)s;"),
+    "acc_rounding_dropped": ("        if (acc)\n            s = dec_d(dtype, rnd_d(dtype, s));", "        if (0)\n            s = dec_d(dtype, rnd_d(dtype, s));"),
+    "acc_rounding_always": ("        if (acc)\n            s = dec_d(dtype, rnd_d(dtype, s));", "        if (1)\n            s = dec_d(dtype, rnd_d(dtype, s));"),
     "mean_over_H_minus_1": ("float ms = ss32 / (float)H;", "float ms = ss32 / (float)(H - 1);"),
     "eps_dropped": ("float v = ms + eps;", "float v = ms;"),
     "eps_outside_sqrt": ("float v = ms + eps;\n        float rstd = 1.0f / sqrtf(v);",
@@ -50,8 +51,8 @@ MUTANTS = {
     "nvfp4_enc_inverted": ("float enc = (dec == 0.0f) ? 0.0f : gs / dec;", "float enc = (dec == 0.0f) ? 0.0f : dec / gs;"),
     "fp8_scale_not_inverted": ("return 1.0f / scale;", "return scale;"),
     "flip_wrong_word": ("if (words[i] == 0x80000000u)", "if (words[i] == 0x00008000u)"),
-    "sum_skips_rank": ("for (int r = 1; r < R; ++r)\n            s = s + dec_d(dtype, in[(int64_t)r * rank_stride + i]);",
-                       "for (int r = 2; r < R; ++r)\n            s = s + dec_d(dtype, in[(int64_t)r * rank_stride + i]);"),
+    "sum_without_rounding": ("out[i] = rnd_d(dtype, rank_sum(dtype, acc, in + i, rank_stride, R));",
+                             "out[i] = (uint16_t)rank_sum(dtype, acc, in + i, rank_stride, R);"),
     "lamport_clear_wrong_slot": ("io[3] = (flag + 2) % 3;", "io[3] = (flag + 1) % 3;"),
     "buffer_size_missing_R": ("out[0] = (int64_t)R * max_tokens * H * elem_bytes;", "out[0] = max_tokens * H * elem_bytes;"),
 }
@@ -77,6 +78,9 @@ PINS = [
     Fz.test_nvfp4_nibble_order_convention,
     Fz.test_nvfp4_roundtrip_bound_random,
     Fz.test_vector_sum_closed_form_and_fp64,
+    Fz.test_element_type_accumulation_worked_value,
+    lambda: Fz.test_element_type_accumulation_is_chained_library_adds(oracle.BF16),
+    Fz.test_vector_sum_element_type_accumulation,
     Fz.test_workspace_sizes_match_page_formula_golden,
     Fz.test_lamport_state_cycles,
 ]
