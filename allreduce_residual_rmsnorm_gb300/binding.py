@@ -40,6 +40,10 @@ AR_VARIANT_WARP_ROW = 1
 AR_VARIANT_CTA_ROW = 2
 AR_VARIANT_BULK_PIPE = 3
 
+# enum ar_accumulate
+AR_ACC_FP32 = 0
+AR_ACC_ELEMENT = 1
+
 AR_MAX_RANKS = 16
 AR_ONESHOT_MAX_TOKENS = 128
 AR_BARRIER_FLAG_COUNT = 256
@@ -116,6 +120,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.ar_fusion_workspace_set_variant.argtypes = [_vp, _i]
     L.ar_fusion_workspace_set_mode.argtypes = [_vp, _i]
     L.ar_fusion_workspace_set_launch.argtypes = [_vp, _i, _i]
+    L.ar_fusion_workspace_set_accumulate.argtypes = [_vp, _i]
+    L.ar_fusion_sum_ex.argtypes = [ctypes.POINTER(_vp), _i, ctypes.c_size_t, _i, _i, _vp, _vp]
     L.ar_fusion_workspace_stage.argtypes = [_vp, _i, _vp, _i, _i, _vp]
     L.ar_fusion_run.argtypes = [_vp, ctypes.POINTER(_vp), _i, _i, _i, _i, _vp, _vp,
                                 ctypes.c_float, _i, _vp, _vp, _vp, _vp, _vp, _vp]
@@ -129,7 +135,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                  "ar_fusion_workspace_copy_state", "ar_fusion_workspace_status",
                  "ar_fusion_workspace_reset", "ar_fusion_workspace_set_timeout_ns",
                  "ar_fusion_workspace_set_variant", "ar_fusion_workspace_set_mode",
-                 "ar_fusion_workspace_set_launch",
+                 "ar_fusion_workspace_set_launch", "ar_fusion_workspace_set_accumulate",
+                 "ar_fusion_sum_ex",
                  "ar_fusion_workspace_stage", "ar_fusion_run", "ar_fusion_norm_amax",
                  "ar_fusion_sum", "ar_fusion_run_noalloc"):
         getattr(L, name).restype = _i
@@ -274,6 +281,10 @@ def ar_fusion_workspace_set_launch(ws: Workspace, cluster_size: int = 0, pdl: in
     _check(lib().ar_fusion_workspace_set_launch(ws.handle, int(cluster_size), int(pdl)))
 
 
+def ar_fusion_workspace_set_accumulate(ws: Workspace, accumulate: int) -> None:
+    _check(lib().ar_fusion_workspace_set_accumulate(ws.handle, int(accumulate)))
+
+
 def ar_fusion_workspace_stage(ws: Workspace, rank: int, src: torch.Tensor, tokens: int | None = None,
                               mode: int = AR_MODE_AUTO, stream=None) -> None:
     if tokens is None:
@@ -313,6 +324,14 @@ def ar_fusion_norm_amax(ws: Workspace, partials, residual_in: torch.Tensor, gamm
     _check(lib().ar_fusion_norm_amax(ws.handle, parr, R, tokens, hidden, _dtype_id(residual_in),
                                      _ptr(residual_in), _ptr(gamma), ctypes.c_float(eps),
                                      _ptr(amax_out), _stream(stream)))
+
+
+def ar_fusion_sum_ex(bufs, out: torch.Tensor, accumulate: int, n: int | None = None,
+                     stream=None) -> None:
+    if n is None:
+        n = out.numel()
+    _check(lib().ar_fusion_sum_ex(_ptr_array(bufs), len(bufs), n, _dtype_id(out), int(accumulate),
+                                  _ptr(out), _stream(stream)))
 
 
 def ar_fusion_sum(bufs, out: torch.Tensor, n: int | None = None, stream=None) -> None:

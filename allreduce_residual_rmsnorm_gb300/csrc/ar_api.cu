@@ -44,6 +44,7 @@ struct ar_fusion_ws {
     int variant, mode, last_variant;
     uint64_t timeout_ns;
     int cluster, pdl;           // launch options of the fused call (0 cluster = auto)
+    int acc;                    // AR_ACC_FP32 or AR_ACC_ELEMENT
 };
 
 namespace {
@@ -305,6 +306,7 @@ int prepare(ar_fusion_ws* ws, const void* const* partials, int nranks, int token
     }
     a.state = state_of(ws);
     a.timeout_ns = ws->timeout_ns;
+    a.acc = ws->acc;
     launch = true;
     return AR_OK;
 }
@@ -409,6 +411,7 @@ int ar_fusion_workspace_create(int tp_size, int max_token_num, int hidden_dim, i
     ws->last_variant = AR_VARIANT_AUTO;
     ws->cluster = 0;
     ws->pdl = 0;
+    ws->acc = AR_ACC_FP32;
     ws->mode = AR_MODE_AUTO;
     ws->timeout_ns = 2000000000ull;
     if (ws->owned) {
@@ -553,6 +556,14 @@ int ar_fusion_workspace_set_launch(ar_fusion_ws* ws, int cluster_size, int pdl)
     return AR_OK;
 }
 
+int ar_fusion_workspace_set_accumulate(ar_fusion_ws* ws, int accumulate)
+{
+    if (!ws || (accumulate != AR_ACC_FP32 && accumulate != AR_ACC_ELEMENT))
+        return fail(AR_ERR_INVALID, "workspace NULL or accumulate %d unknown", accumulate);
+    ws->acc = accumulate;
+    return AR_OK;
+}
+
 int ar_fusion_workspace_set_mode(ar_fusion_ws* ws, int mode)
 {
     if (!ws || mode < AR_MODE_AUTO || mode > AR_MODE_BUFFER)
@@ -642,6 +653,14 @@ int ar_fusion_norm_amax(ar_fusion_ws* ws, const void* const* partials, int nrank
 int ar_fusion_sum(const void* const* bufs, int nranks, size_t n, int dtype, void* out,
                   void* stream)
 {
+    return ar_fusion_sum_ex(bufs, nranks, n, dtype, AR_ACC_FP32, out, stream);
+}
+
+int ar_fusion_sum_ex(const void* const* bufs, int nranks, size_t n, int dtype, int accumulate,
+                     void* out, void* stream)
+{
+    if (accumulate != AR_ACC_FP32 && accumulate != AR_ACC_ELEMENT)
+        return fail(AR_ERR_INVALID, "accumulate %d unknown", accumulate);
     if (dtype != AR_DT_BF16 && dtype != AR_DT_FP16)
         return fail(AR_ERR_UNSUPPORTED, "dtype %d is not bf16 (0) or fp16 (1)", dtype);
     if (nranks < 1 || nranks > AR_MAX_RANKS)
@@ -660,6 +679,7 @@ int ar_fusion_sum(const void* const* bufs, int nranks, size_t n, int dtype, void
     a.out = static_cast<uint8_t*>(out);
     a.R = nranks;
     a.n = n;
+    a.acc = accumulate;
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess)

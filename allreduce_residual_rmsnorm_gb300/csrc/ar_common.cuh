@@ -123,6 +123,13 @@ __device__ __forceinline__ void add8(float (&s)[8], const uint4& v)
     add2<D>(s[6], s[7], v.w);
 }
 
+// s[i] = f(rnd(s[i])): the element-type accumulation rounds every partial sum
+template <class D>
+__device__ __forceinline__ void round8(float (&s)[8])
+{
+    unpack8<D>(pack8<D>(s), s);
+}
+
 // Squares of a packed pair, exact (8- or 11-bit significands): fma with a
 // -0.0 addend, so a zero element gives +0.
 template <class D>

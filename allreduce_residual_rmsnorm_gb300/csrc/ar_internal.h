@@ -27,6 +27,7 @@ struct FusedArgs {
     uint64_t slot_bytes;
     ar_fusion_state* state;     // status word always; slot state in Lamport mode
     uint64_t timeout_ns;
+    int acc;                    // 1: round the rank sum to the element type after every add
 };
 
 struct LaunchCfg {
@@ -47,6 +48,7 @@ struct SumArgs {
     uint8_t* out;
     int R;
     uint64_t n;
+    int acc;                    // 1: round to the element type after every add
 };
 cudaError_t launch_vector_sum(int dtype, const SumArgs& a, const LaunchCfg& c);
 

@@ -225,8 +225,11 @@ fused_pipe_kernel(const FusedArgs a, const int S, const int NC)
             for (int k = 0; k < VPT; ++k) {
                 if (u == 0)
                     unpack8<D>(w[k], acc[k]);
-                else if (u < R)
+                else if (u < R) {
                     add8<D>(acc[k], w[k]);
+                    if (a.acc)
+                        round8<D>(acc[k]);
+                }
                 else
                     xr[k] = w[k];
             }

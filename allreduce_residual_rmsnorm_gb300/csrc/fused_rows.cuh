@@ -193,10 +193,13 @@ fused_rows_kernel(const FusedArgs a)
 #pragma unroll
                         for (int rr = 0; rr < RB; ++rr) {
                             if (r0 + rr < R) {
-                                if (r0 + rr == 0)
+                                if (r0 + rr == 0) {
                                     unpack8<D>(raw[kk][rr], s[kk]);
-                                else
+                                } else {
                                     add8<D>(s[kk], raw[kk][rr]);
+                                    if (a.acc)
+                                        round8<D>(s[kk]);
+                                }
                             }
                         }
                     }

@@ -38,6 +38,16 @@ __device__ __forceinline__ void st_elem(uint8_t* p, uint64_t i, float v)
     reinterpret_cast<uint16_t*>(p)[i] = b;
 }
 
+// f(rnd(v)) in the element type
+template <class D>
+__device__ __forceinline__ float round1(float v)
+{
+    if constexpr (D::id == AR_DT_BF16)
+        return __bfloat162float(__float2bfloat16_rn(v));
+    else
+        return __half2float(__float2half_rn(v));
+}
+
 template <class D, int RMAX>
 __device__ __forceinline__ uint4 sum_vec(const SumArgs& a, const uint4 (&raw)[RMAX])
 {
@@ -51,6 +61,8 @@ __device__ __forceinline__ uint4 sum_vec(const SumArgs& a, const uint4 (&raw)[RM
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 s[i] = __fadd_rn(s[i], t[i]);
+            if (a.acc)
+                round8<D>(s);
         }
     }
     return pack8<D>(s);
@@ -87,8 +99,11 @@ __global__ void __launch_bounds__(256) vector_sum_kernel(const SumArgs a)
     if (tid < tail) {
         const uint64_t e = nvec * 8 + tid;
         float s = ld_elem<D>(a.in[0], e);
-        for (int r = 1; r < a.R; ++r)
+        for (int r = 1; r < a.R; ++r) {
             s = __fadd_rn(s, ld_elem<D>(a.in[r], e));
+            if (a.acc)
+                s = round1<D>(s);
+        }
         st_elem<D>(a.out, e, s);
     }
 }
@@ -99,8 +114,11 @@ __global__ void __launch_bounds__(256) vector_sum_scalar_kernel(const SumArgs a)
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
     for (uint64_t e = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; e < a.n; e += stride) {
         float s = ld_elem<D>(a.in[0], e);
-        for (int r = 1; r < a.R; ++r)
+        for (int r = 1; r < a.R; ++r) {
             s = __fadd_rn(s, ld_elem<D>(a.in[r], e));
+            if (a.acc)
+                s = round1<D>(s);
+        }
         st_elem<D>(a.out, e, s);
     }
 }

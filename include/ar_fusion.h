@@ -85,6 +85,15 @@ enum ar_status {
     AR_ERR_CAPACITY = -5      /* tokens > max_token_num of the workspace */
 };
 
+/* Accumulation of the rank sum (TensorRT-LLM allReduceFusionKernels.cu:
+ * allreduce_sum with Fp32Acc, the default of use_fp32_acc, or chained add128
+ * in the element type; mscclpp allreduce.cu vectorSum adds in the element
+ * type). */
+enum ar_accumulate {
+    AR_ACC_FP32 = 0,          /* fp32, rank order, rounded to the element type once */
+    AR_ACC_ELEMENT = 1        /* rounded to the element type after every addition */
+};
+
 /* Where ar_fusion_run reads the partials from when `partials` is NULL. */
 enum ar_mode {
     AR_MODE_AUTO = 0,         /* tokens <= AR_ONESHOT_MAX_TOKENS -> LAMPORT, else BUFFER */
@@ -223,6 +232,10 @@ int ar_fusion_workspace_set_mode(ar_fusion_ws* ws, int mode);
  * waits on the device for its results.  Errors: AR_ERR_INVALID. */
 int ar_fusion_workspace_set_launch(ar_fusion_ws* ws, int cluster_size, int pdl);
 
+/* Accumulation of the rank sum of later fused calls (enum ar_accumulate;
+ * default AR_ACC_FP32).  Host-side; no CUDA call.  Errors: AR_ERR_INVALID. */
+int ar_fusion_workspace_set_accumulate(ar_fusion_ws* ws, int accumulate);
+
 /* Stage rank `rank`'s partial [tokens][hidden] (device pointer `src`) into the
  * workspace, standing in for the one-shot push of
  * allreduce_fusion_kernel_oneshot_lamport (on one GPU nothing is pushed over
@@ -297,6 +310,13 @@ int ar_fusion_norm_amax(ar_fusion_ws* ws, const void* const* partials, int nrank
  * 128-bit path.  Errors: AR_ERR_INVALID, AR_ERR_UNSUPPORTED, AR_ERR_CUDA. */
 int ar_fusion_sum(const void* const* bufs, int nranks, size_t n, int dtype, void* out,
                   void* stream);
+
+/* ar_fusion_sum with a choice of accumulation (enum ar_accumulate):
+ * AR_ACC_ELEMENT rounds every partial sum to the element type, as mscclpp's
+ * vectorSum does with half-precision adds.  ar_fusion_sum is AR_ACC_FP32.
+ * Errors as ar_fusion_sum, and AR_ERR_INVALID for an unknown accumulate. */
+int ar_fusion_sum_ex(const void* const* bufs, int nranks, size_t n, int dtype, int accumulate,
+                     void* out, void* stream);
 
 /* ------------------------------------------------- no-allocation call -- */
 

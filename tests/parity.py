@@ -23,14 +23,16 @@ def to_float(bits16: np.ndarray, dtype: str) -> np.ndarray:
     return W.from_bits(bits16, dtype).float().numpy()
 
 
-def oracle_expected(w: W.FusedWorkload, inp: W.FusedInputs, lamport_flip: bool = False):
+def oracle_expected(w: W.FusedWorkload, inp: W.FusedInputs, lamport_flip: bool = False,
+                    acc: int = 0):
     """Oracle outputs for the workload: dict with residual, norm, amax and,
     when quantised, the scale passed to both sides and the codes."""
     odt = ODT[w.dtype]
     P = W.bits(inp.partials)
     if lamport_flip:
         P = oracle.lamport_flip(P)
-    res, nrm, rstd = oracle.fused(odt, P, W.bits(inp.residual), W.bits(inp.gamma), inp.eps)
+    res, nrm, rstd = oracle.fused(odt, P, W.bits(inp.residual), W.bits(inp.gamma), inp.eps,
+                                  acc=acc)
     out = {"residual": res, "norm": nrm, "rstd": rstd}
     pat = B.PATTERNS[w.pattern]
     if pat & (B.AR_QUANT_FP8 | B.AR_QUANT_NVFP4):

@@ -91,6 +91,7 @@ def test_run_and_calls_reject_null_workspace(L):
     assert L.ar_fusion_workspace_set_variant(None, 1) == B.AR_ERR_INVALID
     assert L.ar_fusion_workspace_set_mode(None, 1) == B.AR_ERR_INVALID
     assert L.ar_fusion_workspace_set_launch(None, 2, 1) == B.AR_ERR_INVALID
+    assert L.ar_fusion_workspace_set_accumulate(None, 1) == B.AR_ERR_INVALID
     assert L.ar_fusion_workspace_set_timeout_ns(None, 5) == B.AR_ERR_INVALID
     assert L.ar_fusion_workspace_destroy(None) == B.AR_OK
 
@@ -101,6 +102,7 @@ def test_sum_validation(L):
     assert L.ar_fusion_sum(arr, 17, 10, 0, ctypes.c_void_p(64), None) == B.AR_ERR_UNSUPPORTED
     assert L.ar_fusion_sum(arr, 2, 10, 3, ctypes.c_void_p(64), None) == B.AR_ERR_UNSUPPORTED
     assert L.ar_fusion_sum(arr, 2, 0, 0, ctypes.c_void_p(64), None) == B.AR_OK     # empty: no launch
+    assert L.ar_fusion_sum_ex(arr, 2, 10, 0, 7, ctypes.c_void_p(64), None) == B.AR_ERR_INVALID
     assert L.ar_fusion_sum(arr, 2, 10, 0, None, None) == B.AR_ERR_INVALID
     bad = (ctypes.c_void_p * 2)(16, 33)
     assert L.ar_fusion_sum(bad, 2, 10, 0, ctypes.c_void_p(64), None) == B.AR_ERR_INVALID

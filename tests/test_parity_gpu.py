@@ -22,15 +22,16 @@ def make_ws(w, max_tokens=None, mem=False):
 
 
 def run_and_check(w, variant=B.AR_VARIANT_AUTO, staged=False, mode=B.AR_MODE_AUTO, inp=None,
-                  max_tokens=None, cluster=0, pdl=0):
+                  max_tokens=None, cluster=0, pdl=0, acc=B.AR_ACC_FP32):
     inp = inp or W.make_fused_inputs(w)
     ws = make_ws(w, max_tokens)
     B.ar_fusion_workspace_set_variant(ws, variant)
     B.ar_fusion_workspace_set_mode(ws, mode)
     B.ar_fusion_workspace_set_launch(ws, cluster, pdl)
+    B.ar_fusion_workspace_set_accumulate(ws, acc)
     lam = staged and (mode == B.AR_MODE_LAMPORT or
                       (mode == B.AR_MODE_AUTO and w.T <= B.AR_ONESHOT_MAX_TOKENS))
-    exp = PY.oracle_expected(w, inp, lamport_flip=lam)
+    exp = PY.oracle_expected(w, inp, lamport_flip=lam, acc=acc)
     got = PY.run_gpu(ws, w, inp, scale=exp.get("scale"), staged=staged)
     rc, detail = B.ar_fusion_workspace_status(ws)
     assert rc == 0, (rc, detail)
@@ -145,6 +146,39 @@ def test_set_launch_rejects_bad_values():
             B.ar_fusion_workspace_set_launch(ws, cl, pdl)
         assert e.value.code == B.AR_ERR_INVALID
     B.ar_fusion_workspace_destroy(ws)
+
+
+# ---------------------------------------- element-type accumulation variant
+
+ACC_CASES = [
+    (W.TINY, B.AR_VARIANT_WARP_ROW, True),
+    (W.DECODE, B.AR_VARIANT_CTA_ROW, True),
+    (W.FusedWorkload("acc_fp16", R=5, T=300, H=3072, dtype="fp16", pattern=W.RES_NORM_FP8),
+     B.AR_VARIANT_CTA_ROW, False),
+    (W.FusedWorkload("acc_pipe", R=8, T=400, H=7168, pattern=W.RES_QUANT_NVFP4, heavy_frac=0.01),
+     B.AR_VARIANT_BULK_PIPE, False),
+    (W.FusedWorkload("acc_r16", R=16, T=33, H=1024, pattern=W.RES_NORM), B.AR_VARIANT_WARP_ROW, False),
+]
+
+
+@pytest.mark.parametrize("w,variant,staged", ACC_CASES, ids=lambda x: getattr(x, "name", str(x)))
+def test_element_type_accumulation(w, variant, staged):
+    stats, _, _ = run_and_check(w, variant, staged, acc=B.AR_ACC_ELEMENT)
+    assert stats.get("residual_mismatch", 0) == 0, stats
+    assert stats.get("norm_mismatch", 0) <= max(1, w.T * w.H // 100000), stats
+
+
+@pytest.mark.parametrize("R,N,dtype,offset", [(8, 1_000_003, "fp16", 0), (3, 4099, "bf16", 0),
+                                               (16, 77777, "fp16", 1)])
+def test_vector_sum_element_type_accumulation(R, N, dtype, offset):
+    x = W.make_sum_inputs(W.SumWorkload("s", R=R, N=N + offset, dtype=dtype))
+    exp = oracle.vector_sum(PY.ODT[dtype], W.bits(x[:, offset:]), acc=1)
+    xd = x.cuda()
+    out_full = torch.zeros(N + 8, dtype=xd.dtype, device="cuda")
+    out = out_full[offset:offset + N]
+    B.ar_fusion_sum_ex([xd[r, offset:] for r in range(R)], out, B.AR_ACC_ELEMENT)
+    torch.cuda.synchronize()
+    assert np.array_equal(W.bits(out.cpu()), exp)
 
 
 @pytest.mark.parametrize("staged", [False, True])
