@@ -36,7 +36,35 @@ constexpr int rows_max_threads()
     return WARP_ROW ? 256 : (VPT == 1 ? (RMAX <= 4 ? 1024 : 896) : 512);
 }
 
-template <class D, int RMAX, int VPT, bool WARP_ROW>
+// s[kk] (+)= rank batch r0..r0+RB-1 of vector g + (k0 + kk) * G; ELEM rounds
+// every partial sum to the element type.
+template <class D, int KCH, int RB, bool ELEM>
+__device__ __forceinline__ void fold_ranks(float (&s)[KCH][8], const uint4 (&raw)[KCH][RB], int r0,
+                                           int R, int g, int k0, int G, int Hv)
+{
+#pragma unroll
+    for (int kk = 0; kk < KCH; ++kk) {
+        if (g + (k0 + kk) * G < Hv) {
+#pragma unroll
+            for (int rr = 0; rr < RB; ++rr) {
+                if (r0 + rr < R) {
+                    if (r0 + rr == 0) {
+                        unpack8<D>(raw[kk][rr], s[kk]);
+                    } else {
+                        add8<D>(s[kk], raw[kk][rr]);
+                        if (ELEM)
+                            round8<D>(s[kk]);
+                    }
+                }
+            }
+        }
+    }
+}
+
+// CLUSTER: the kernel is launched with a thread-block cluster and one row
+// spans its CTAs (a separate instantiation, so the common one-CTA-per-row
+// kernel carries none of the cluster code).
+template <class D, int RMAX, int VPT, bool WARP_ROW, bool CLUSTER = false>
 __global__ void __launch_bounds__(rows_max_threads<RMAX, VPT, WARP_ROW>())
 fused_rows_kernel(const FusedArgs a)
 {
@@ -60,15 +88,20 @@ fused_rows_kernel(const FusedArgs a)
         g = lane;
         row = blockIdx.x * nwarps + warp;
         row_step = gridDim.x * nwarps;
+    } else if (!CLUSTER) {
+        G = blockDim.x;
+        g = threadIdx.x;
+        row = blockIdx.x;
+        row_step = gridDim.x;
     } else {
-        // one row per cluster of C CTAs (C = 1 without a cluster launch):
-        // CTA `crank` holds vectors [crank * blockDim, (crank + 1) * blockDim)
+        // one row per cluster of C CTAs: CTA `crank` holds vectors
+        // [crank * blockDim, (crank + 1) * blockDim)
         G = blockDim.x * cluster_size();
         g = cluster_rank() * blockDim.x + threadIdx.x;
         row = cluster_id();
         row_step = cluster_count();
     }
-    const unsigned C = WARP_ROW ? 1u : cluster_size();
+    const unsigned C = CLUSTER ? cluster_size() : 1u;
 
     // inputs and the slot state may be written by the preceding grid
     pdl_wait();
@@ -186,24 +219,12 @@ fused_rows_kernel(const FusedArgs a)
                         }
                     }
                 }
-                // ---- fold this rank batch into the fp32 sum (rank order)
-#pragma unroll
-                for (int kk = 0; kk < KCH; ++kk) {
-                    if (g + (k0 + kk) * G < Hv) {
-#pragma unroll
-                        for (int rr = 0; rr < RB; ++rr) {
-                            if (r0 + rr < R) {
-                                if (r0 + rr == 0) {
-                                    unpack8<D>(raw[kk][rr], s[kk]);
-                                } else {
-                                    add8<D>(s[kk], raw[kk][rr]);
-                                    if (a.acc)
-                                        round8<D>(s[kk]);
-                                }
-                            }
-                        }
-                    }
-                }
+                // ---- fold this rank batch into the fp32 sum (rank order); the
+                // accumulation choice is taken once, outside the unrolled fold
+                if (!a.acc)
+                    fold_ranks<D, KCH, RB, false>(s, raw, r0, R, g, k0, G, Hv);
+                else
+                    fold_ranks<D, KCH, RB, true>(s, raw, r0, R, g, k0, G, Hv);
             }
             // ---- residual add, sum of squares
 #pragma unroll
@@ -225,7 +246,7 @@ fused_rows_kernel(const FusedArgs a)
         float rstd;
         if (WARP_ROW) {
             rstd = inv_rms(df_warp_sum(ss), H, a.eps);
-        } else if (C == 1) {
+        } else if (!CLUSTER) {
             rstd = row_rstd(ss, red[parity], &rstd_sh[parity], warp, lane, nwarps, H, a.eps,
                             BlockSync{});
             parity ^= 1;
@@ -269,7 +290,7 @@ fused_rows_kernel(const FusedArgs a)
 
     // no CTA may leave while another CTA of its cluster can still read its
     // row partial
-    if (C > 1)
+    if (CLUSTER)
         cluster_barrier();
     pdl_trigger();
 

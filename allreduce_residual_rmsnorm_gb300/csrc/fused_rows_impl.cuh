@@ -26,6 +26,19 @@ static const void* rows_fn_vpt(int vpt)
     }
 }
 
+// one-vector-per-thread row kernels launched with a cluster
+template <class D>
+static const void* rows_cluster_fn(int rmax)
+{
+    switch (rmax) {
+    case 2: return (const void*)fused_rows_kernel<D, 2, 1, false, true>;
+    case 4: return (const void*)fused_rows_kernel<D, 4, 1, false, true>;
+    case 8: return (const void*)fused_rows_kernel<D, 8, 1, false, true>;
+    case 16: return (const void*)fused_rows_kernel<D, 16, 1, false, true>;
+    default: return nullptr;
+    }
+}
+
 template <class D, bool WARP_ROW>
 static const void* rows_fn(int rmax, int vpt)
 {
@@ -128,7 +141,9 @@ cudaError_t launch_fused_rows_t(int variant, const FusedArgs& a, const LaunchCfg
         const int vpt = (Hv + C - 1) / C <= one_vec_max ? 1 : pow2_at_least((Hv + 511) / 512);
         if (vpt > 8)
             return cudaErrorInvalidValue;
-        fn = rows_fn<D, false>(rmax, vpt);
+        fn = (C > 1 && vpt == 1) ? rows_cluster_fn<D>(rmax) : rows_fn<D, false>(rmax, vpt);
+        if (vpt != 1)
+            C = 1;
         threads = ((Hv + C * vpt - 1) / (C * vpt) + 31) / 32 * 32;
         if (C == 1) {
             const int cap = c.sms * blocks_per_sm(fn, threads);
