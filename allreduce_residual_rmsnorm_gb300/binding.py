@@ -40,6 +40,9 @@ AR_VARIANT_WARP_ROW = 1
 AR_VARIANT_CTA_ROW = 2
 AR_VARIANT_BULK_PIPE = 3
 
+# enum ar_scale_layout
+AR_SF_LINEAR = 0
+AR_SF_SWIZZLED = 1
 # enum ar_accumulate
 AR_ACC_FP32 = 0
 AR_ACC_ELEMENT = 1
@@ -121,6 +124,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.ar_fusion_workspace_set_mode.argtypes = [_vp, _i]
     L.ar_fusion_workspace_set_launch.argtypes = [_vp, _i, _i]
     L.ar_fusion_workspace_set_accumulate.argtypes = [_vp, _i]
+    L.ar_fusion_workspace_set_scale_layout.argtypes = [_vp, _i]
     L.ar_fusion_sum_ex.argtypes = [ctypes.POINTER(_vp), _i, ctypes.c_size_t, _i, _i, _vp, _vp]
     L.ar_fusion_workspace_stage.argtypes = [_vp, _i, _vp, _i, _i, _vp]
     L.ar_fusion_run.argtypes = [_vp, ctypes.POINTER(_vp), _i, _i, _i, _i, _vp, _vp,
@@ -136,6 +140,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                  "ar_fusion_workspace_reset", "ar_fusion_workspace_set_timeout_ns",
                  "ar_fusion_workspace_set_variant", "ar_fusion_workspace_set_mode",
                  "ar_fusion_workspace_set_launch", "ar_fusion_workspace_set_accumulate",
+                 "ar_fusion_workspace_set_scale_layout",
                  "ar_fusion_sum_ex",
                  "ar_fusion_workspace_stage", "ar_fusion_run", "ar_fusion_norm_amax",
                  "ar_fusion_sum", "ar_fusion_run_noalloc"):
@@ -283,6 +288,16 @@ def ar_fusion_workspace_set_launch(ws: Workspace, cluster_size: int = 0, pdl: in
 
 def ar_fusion_workspace_set_accumulate(ws: Workspace, accumulate: int) -> None:
     _check(lib().ar_fusion_workspace_set_accumulate(ws.handle, int(accumulate)))
+
+
+def ar_fusion_workspace_set_scale_layout(ws: Workspace, layout: int) -> None:
+    _check(lib().ar_fusion_workspace_set_scale_layout(ws.handle, int(layout)))
+
+
+def swizzled_scale_bytes(tokens: int, hidden: int) -> int:
+    """Size of an AR_SF_SWIZZLED scale buffer (whole 128 x 4 tiles)."""
+    kb = hidden // 16
+    return (tokens + 127) // 128 * 128 * ((kb + 3) // 4) * 4
 
 
 def ar_fusion_workspace_stage(ws: Workspace, rank: int, src: torch.Tensor, tokens: int | None = None,

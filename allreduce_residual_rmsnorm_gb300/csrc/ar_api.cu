@@ -45,6 +45,7 @@ struct ar_fusion_ws {
     uint64_t timeout_ns;
     int cluster, pdl;           // launch options of the fused call (0 cluster = auto)
     int acc;                    // AR_ACC_FP32 or AR_ACC_ELEMENT
+    int sf_layout;              // AR_SF_LINEAR or AR_SF_SWIZZLED
 };
 
 namespace {
@@ -307,6 +308,7 @@ int prepare(ar_fusion_ws* ws, const void* const* partials, int nranks, int token
     a.state = state_of(ws);
     a.timeout_ns = ws->timeout_ns;
     a.acc = ws->acc;
+    a.sf_layout = ws->sf_layout;
     launch = true;
     return AR_OK;
 }
@@ -412,6 +414,7 @@ int ar_fusion_workspace_create(int tp_size, int max_token_num, int hidden_dim, i
     ws->cluster = 0;
     ws->pdl = 0;
     ws->acc = AR_ACC_FP32;
+    ws->sf_layout = AR_SF_LINEAR;
     ws->mode = AR_MODE_AUTO;
     ws->timeout_ns = 2000000000ull;
     if (ws->owned) {
@@ -561,6 +564,14 @@ int ar_fusion_workspace_set_accumulate(ar_fusion_ws* ws, int accumulate)
     if (!ws || (accumulate != AR_ACC_FP32 && accumulate != AR_ACC_ELEMENT))
         return fail(AR_ERR_INVALID, "workspace NULL or accumulate %d unknown", accumulate);
     ws->acc = accumulate;
+    return AR_OK;
+}
+
+int ar_fusion_workspace_set_scale_layout(ar_fusion_ws* ws, int layout)
+{
+    if (!ws || (layout != AR_SF_LINEAR && layout != AR_SF_SWIZZLED))
+        return fail(AR_ERR_INVALID, "workspace NULL or scale layout %d unknown", layout);
+    ws->sf_layout = layout;
     return AR_OK;
 }
 

@@ -28,6 +28,7 @@ struct FusedArgs {
     ar_fusion_state* state;     // status word always; slot state in Lamport mode
     uint64_t timeout_ns;
     int acc;                    // 1: round the rank sum to the element type after every add
+    int sf_layout;              // NVFP4 scale bytes: AR_SF_LINEAR or AR_SF_SWIZZLED
 };
 
 struct LaunchCfg {

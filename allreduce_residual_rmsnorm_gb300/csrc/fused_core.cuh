@@ -88,6 +88,20 @@ __device__ __forceinline__ void load_gamma(const uint8_t* gamma, int v, bool ok,
     }
 }
 
+// Byte offset of NVFP4 block scale (row m, block k) of a [T][H/16] scale
+// matrix: linear row-major, or tiles of 128 rows x 4 blocks (512 bytes each,
+// tiles row-major over (m / 128, k / 4)) holding row m at
+// (m % 32) * 16 + ((m / 32) % 4) * 4 + k % 4 -- the block-scale layout that
+// tensor-core NVFP4 matrix multiplies read.
+__device__ __forceinline__ size_t sf_offset(int layout, int m, int k, int kblocks)
+{
+    if (layout == AR_SF_LINEAR)
+        return (size_t)m * kblocks + k;
+    const size_t ktiles = (size_t)(kblocks + 3) / 4;
+    const size_t tile = (size_t)(m >> 7) * ktiles + (size_t)(k >> 2);
+    return tile * 512 + (size_t)(m & 31) * 16 + (size_t)((m >> 5) & 3) * 4 + (size_t)(k & 3);
+}
+
 // n = rnd((f(y) * rstd) * gamma); stores norm_out and the quantised outputs
 // of vector v of `row`.  Every lane of the warp must call this (the NVFP4
 // block maximum is exchanged with the xor-1 neighbour); `ok` masks the stores
@@ -140,7 +154,7 @@ __device__ __forceinline__ void normalize_vec(const FusedArgs& a, int pat, int r
         if (ok) {
             *reinterpret_cast<uint32_t*>(a.quant_out + (size_t)row * (H / 2) + (size_t)v * 4) = codes;
             if ((v & 1) == 0)
-                a.scale_out[(size_t)row * (H / 16) + (v >> 1)] = (uint8_t)sf;
+                a.scale_out[sf_offset(a.sf_layout, row, v >> 1, H / 16)] = (uint8_t)sf;
         }
     }
 }

@@ -94,6 +94,12 @@ enum ar_accumulate {
     AR_ACC_ELEMENT = 1        /* rounded to the element type after every addition */
 };
 
+/* Layout of the NVFP4 block-scale bytes (scale_out). */
+enum ar_scale_layout {
+    AR_SF_LINEAR = 0,         /* [tokens][hidden/16], row-major */
+    AR_SF_SWIZZLED = 1        /* tiles of 128 rows x 4 blocks, see ar_fusion_workspace_set_scale_layout */
+};
+
 /* Where ar_fusion_run reads the partials from when `partials` is NULL. */
 enum ar_mode {
     AR_MODE_AUTO = 0,         /* tokens <= AR_ONESHOT_MAX_TOKENS -> LAMPORT, else BUFFER */
@@ -235,6 +241,18 @@ int ar_fusion_workspace_set_launch(ar_fusion_ws* ws, int cluster_size, int pdl);
 /* Accumulation of the rank sum of later fused calls (enum ar_accumulate;
  * default AR_ACC_FP32).  Host-side; no CUDA call.  Errors: AR_ERR_INVALID. */
 int ar_fusion_workspace_set_accumulate(ar_fusion_ws* ws, int accumulate);
+
+/* Layout of the NVFP4 scale bytes written by later fused calls (enum
+ * ar_scale_layout; default AR_SF_LINEAR).  TensorRT-LLM's fused_op writes the
+ * scales through cvt_quant_to_fp4_get_sf_out_offset, a header that is not on
+ * the pages; AR_SF_SWIZZLED is the block-scale layout that tensor-core NVFP4
+ * matrix multiplies consume: with kb = hidden/16 blocks per row and
+ * kt = ceil(kb / 4), the scale of (row m, block k) is at byte
+ *     ((m / 128) * kt + k / 4) * 512 + (m % 32) * 16 + ((m / 32) % 4) * 4 + k % 4
+ * so scale_out must hold ceil(tokens / 128) * 128 * kt * 4 bytes; padding
+ * bytes (rows >= tokens, blocks >= kb) are not written -- zero them once if
+ * the consumer reads them.  Host-side; no CUDA call.  Errors: AR_ERR_INVALID. */
+int ar_fusion_workspace_set_scale_layout(ar_fusion_ws* ws, int layout);
 
 /* Stage rank `rank`'s partial [tokens][hidden] (device pointer `src`) into the
  * workspace, standing in for the one-shot push of

@@ -368,6 +368,25 @@ void oracle_quant_nvfp4(int dtype, const uint16_t* n_in, int64_t T, int64_t H, f
     }
 }
 
+/* NVFP4 block scales of a [T][KB] matrix rearranged into tiles of 128 rows x
+ * 4 blocks, as tensor-core NVFP4 matrix multiplies read them (a layout of
+ * ours to match that consumer; the pages' helper header is absent): tiles are
+ * ordered row-major over (row / 128, block / 4), 512 bytes each, and inside a
+ * tile row m, block k sits at (m % 32) * 16 + ((m / 32) % 4) * 4 + k % 4.
+ * `out` has ceil(T / 128) * 128 * ceil(KB / 4) * 4 bytes; bytes that belong to
+ * no (m < T, k < KB) are left as they are. */
+void oracle_swizzle_scales(const uint8_t* linear, int64_t T, int64_t KB, uint8_t* out)
+{
+    int64_t ktiles = (KB + 3) / 4;
+    for (int64_t m = 0; m < T; ++m) {
+        for (int64_t k = 0; k < KB; ++k) {
+            int64_t tile = (m / 128) * ktiles + k / 4;
+            int64_t within = (m % 32) * 16 + ((m / 32) % 4) * 4 + k % 4;
+            out[tile * 512 + within] = linear[m * KB + k];
+        }
+    }
+}
+
 /* ------------------------------------------------------- plain R-way sum --- */
 
 /* out_i = rnd_D(f(in_0[i]) + f(in_1[i]) + ... + f(in_{R-1}[i])), fp32, rank

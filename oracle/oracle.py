@@ -24,7 +24,7 @@ __all__ = [
     "e4m3_encode", "e4m3_decode", "e2m1_encode", "e2m1_decode",
     "lamport_flip", "fused", "amax", "fp8_inv_scale", "quant_fp8",
     "nvfp4_global_scale", "quant_nvfp4", "vector_sum", "workspace_sizes",
-    "lamport_step", "host_threads",
+    "lamport_step", "host_threads", "swizzle_scales",
 ]
 
 BF16 = 0
@@ -100,6 +100,8 @@ def load_library(path: str) -> ctypes.CDLL:
                                          ctypes.c_int, ctypes.c_int64, ctypes.c_int64, _i64p]
     L.oracle_workspace_sizes.restype = None
     L.oracle_lamport_step.argtypes = [_i64p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64]
+    L.oracle_swizzle_scales.argtypes = [_u8p, ctypes.c_int64, ctypes.c_int64, _u8p]
+    L.oracle_swizzle_scales.restype = None
     L.oracle_lamport_step.restype = None
     return L
 
@@ -281,3 +283,12 @@ def lamport_step(flag: int, clear_size: int, R: int, T: int, H: int):
     io = np.array([flag, clear_size, 0, 0], np.int64)
     lib().oracle_lamport_step(io, R, T, H)
     return int(io[0]), int(io[1]), int(io[2]), int(io[3])
+
+
+def swizzle_scales(linear: np.ndarray) -> np.ndarray:
+    """[T, KB] uint8 block scales -> the 128 x 4 tile layout (zero padding)."""
+    linear = np.ascontiguousarray(linear, dtype=np.uint8)
+    T, KB = linear.shape
+    out = np.zeros((T + 127) // 128 * 128 * ((KB + 3) // 4) * 4, np.uint8)
+    lib().oracle_swizzle_scales(linear, T, KB, out)
+    return out

@@ -378,3 +378,43 @@ def test_lamport_state_cycles():
         seen.append((rd, cl, flag))
         assert clear == 2 * 16 * 512
     assert seen[:4] == [(0, 2, 1), (1, 0, 2), (2, 1, 0), (0, 2, 1)]
+
+
+# ------------------------------------------------- NVFP4 scale tile layout
+
+@pytest.mark.parametrize("T,KB", [(1, 1), (128, 4), (200, 28), (257, 448), (300, 5)])
+def test_swizzled_scales_are_a_tile_permutation(T, KB):
+    # every (row, block) lands on its own byte; whole 128 x 4 tiles are
+    # contiguous 512-byte ranges; the padded buffer holds exactly the tiles
+    lin = np.arange(T * KB, dtype=np.int64)
+    out = oracle.swizzle_scales(np.ones((T, KB), np.uint8))
+    Tp, KBp = (T + 127) // 128 * 128, (KB + 3) // 4 * 4
+    assert out.size == Tp * KBp
+    # a distinct 24-bit tag per cell, carried in three byte planes
+    planes = [oracle.swizzle_scales(((lin >> (8 * i)) & 0xff).astype(np.uint8).reshape(T, KB))
+              for i in range(3)]
+    present = oracle.swizzle_scales(np.ones((T, KB), np.uint8))
+    tags = sum(p.astype(np.int64) << (8 * i) for i, p in enumerate(planes))
+    assert present.sum() == T * KB
+    assert np.array_equal(np.sort(tags[present == 1]), lin)
+    # tile (rb, kb) of the linear matrix occupies bytes [512 t, 512 t + 512)
+    ktiles = KBp // 4
+    for rb in range((T + 127) // 128):
+        for kt in range(ktiles):
+            t = rb * ktiles + kt
+            rows = np.arange(rb * 128, min(T, rb * 128 + 128))
+            cols = np.arange(kt * 4, min(KB, kt * 4 + 4))
+            if rows.size == 0 or cols.size == 0:
+                continue
+            cell = (rows[:, None] * KB + cols[None, :]).ravel()
+            got = tags[t * 512:(t + 1) * 512][present[t * 512:(t + 1) * 512] == 1]
+            assert np.array_equal(np.sort(got), np.sort(cell))
+
+
+def test_swizzled_scales_worked_positions():
+    # within a tile: row 0 block 0 -> 0, row 1 -> 16, row 32 -> 4, row 96 block 3 -> 15,
+    # row 31 block 2 -> 31*16 + 2; next tile along the blocks starts at 512
+    ids = np.zeros((128, 8), np.uint8)
+    ids[0, 0], ids[1, 0], ids[32, 0], ids[96, 3], ids[31, 2], ids[0, 4] = 1, 2, 3, 4, 5, 6
+    out = oracle.swizzle_scales(ids)
+    assert (out[0], out[16], out[4], out[15], out[31 * 16 + 2], out[512]) == (1, 2, 3, 4, 5, 6)

@@ -462,3 +462,81 @@ def test_vector_sum_ranks_types_and_misaligned(R, N, dtype, offset):
     torch.cuda.synchronize()
     assert np.array_equal(W.bits(out.cpu()), exp)
     assert bool((out_full[offset + N:] == 0).all())
+
+
+# ------------------------------------------- NVFP4 scales in the tile layout
+
+def _run_nvfp4_swizzled(w, variant, inp=None, gs=None):
+    inp = inp or W.make_fused_inputs(w)
+    exp = PY.oracle_expected(w, inp)
+    gs = exp["scale"] if gs is None else gs
+    ws = make_ws(w)
+    B.ar_fusion_workspace_set_variant(ws, variant)
+    B.ar_fusion_workspace_set_scale_layout(ws, B.AR_SF_SWIZZLED)
+    P = inp.partials.cuda()
+    X, G = inp.residual.cuda(), inp.gamma.cuda()
+    res = torch.empty_like(X)
+    nrm = torch.empty_like(X)
+    q = torch.zeros(w.T, w.H // 2, dtype=torch.uint8, device="cuda")
+    sf = torch.zeros(B.swizzled_scale_bytes(w.T, w.H), dtype=torch.uint8, device="cuda")
+    sc = torch.tensor([gs], dtype=torch.float32, device="cuda")
+    B.ar_fusion_run(ws, [P[r] for r in range(w.R)], X, G, w.eps, B.PATTERNS[w.pattern],
+                    residual_out=res, norm_out=nrm, quant_out=q, scale_out=sf, scale_factor=sc)
+    torch.cuda.synchronize()
+    B.ar_fusion_workspace_destroy(ws)
+    return exp, q, sf
+
+
+@pytest.mark.parametrize("variant", [B.AR_VARIANT_WARP_ROW, B.AR_VARIANT_CTA_ROW, B.AR_VARIANT_BULK_PIPE])
+@pytest.mark.parametrize("T,H", [(200, 512), (300, 7168), (128, 1040)])
+def test_nvfp4_swizzled_scale_layout_matches_oracle(variant, T, H):
+    w = W.FusedWorkload("swz", R=4, T=T, H=H, pattern=W.RES_NORM_NVFP4, heavy_frac=0.01, seed=T + H)
+    exp, q, sf = _run_nvfp4_swizzled(w, variant)
+    assert np.array_equal(q.cpu().numpy(), exp["quant"])
+    assert np.array_equal(sf.cpu().numpy(), oracle.swizzle_scales(exp["sf"]))
+
+
+def _scaled_mm_nvfp4(a_codes, a_sf_swz, b_codes, b_sf_swz):
+    """NVFP4 x NVFP4 -> bf16 through PyTorch's block-scaled matmul (cuBLASLt),
+    A [M, K/2] and B [N, K/2] packed codes, scales in the tile layout."""
+    fp4 = getattr(torch, "float4_e2m1fn_x2", None)
+    if fp4 is None:
+        pytest.skip("this PyTorch has no float4_e2m1fn_x2")
+    a = a_codes.view(fp4)
+    b = b_codes.view(fp4).t()
+    sa = a_sf_swz.view(torch.float8_e4m3fn)
+    sb = b_sf_swz.view(torch.float8_e4m3fn)
+    F = torch.nn.functional
+    errors = []
+    if hasattr(F, "scaled_mm") and hasattr(F, "ScalingType"):
+        try:
+            return F.scaled_mm(a, b, sa, F.ScalingType.BlockWise1x16, sb, F.ScalingType.BlockWise1x16,
+                               swizzle_a=F.SwizzleType.SWIZZLE_32_4_4,
+                               swizzle_b=F.SwizzleType.SWIZZLE_32_4_4, output_dtype=torch.bfloat16)
+        except Exception as e:  # noqa: BLE001
+            errors.append(repr(e))
+    try:
+        return torch._scaled_mm(a, b, sa, sb, out_dtype=torch.bfloat16)
+    except Exception as e:  # noqa: BLE001
+        errors.append(repr(e))
+    pytest.skip("no usable NVFP4 block-scaled matmul in this PyTorch: " + " | ".join(errors)[:300])
+
+
+@pytest.mark.parametrize("T", [256, 200])
+def test_nvfp4_swizzled_output_feeds_a_block_scaled_matmul(T):
+    # Independent consumer of both the codes (nibble order included) and the
+    # tile layout: with B = identity in NVFP4 (code 1.0, every block scale 1.0)
+    # the product is A's dequantised matrix val(code) * blockscale, exact in
+    # bf16 -- any misplaced scale byte or swapped nibble changes it.
+    H = 512
+    w = W.FusedWorkload("swz_mm", R=8, T=T, H=H, pattern=W.RES_NORM_NVFP4, heavy_frac=0.01, seed=T)
+    exp, q, sf = _run_nvfp4_swizzled(w, B.AR_VARIANT_CTA_ROW)
+    codes = np.stack([exp["quant"] & 0xf, exp["quant"] >> 4], -1).reshape(T, H)
+    deq = oracle.e2m1_decode(codes) * np.repeat(oracle.e4m3_decode(exp["sf"]), 16, axis=1)
+    eye_codes = np.zeros((H, H), np.uint8)
+    np.fill_diagonal(eye_codes, 0x2)                                  # E2M1 1.0
+    b_packed = (eye_codes[:, 0::2] | (eye_codes[:, 1::2] << 4)).astype(np.uint8)
+    b_sf = oracle.swizzle_scales(np.full((H, H // 16), 0x38, np.uint8))  # E4M3 1.0
+    out = _scaled_mm_nvfp4(q, sf, torch.from_numpy(b_packed).cuda(), torch.from_numpy(b_sf).cuda())
+    got = out.float().cpu().numpy()
+    assert np.array_equal(got, deq.astype(np.float32))
