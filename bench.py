@@ -41,6 +41,8 @@ def parse():
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--e2e-steps", type=int, default=None)
+    p.add_argument("--e2e-chunks", type=int, default=8,
+                   help="row chunks of the pipelined end-to-end step (1 = no pipelining)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--variant", default="auto", choices=["auto", "cta", "pipe", "warp"])
     p.add_argument("--tokens", type=int, default=None,
@@ -476,14 +478,33 @@ def main():
     q_h = torch.empty(q.shape, dtype=q.dtype).pin_memory()
     sf_h = torch.empty(sf.shape, dtype=sf.dtype).pin_memory()
 
+    # Rows are independent, so one step is pipelined in row chunks over three
+    # streams: copy a chunk's inputs in (all R partial planes + residual),
+    # run the fused call on that chunk (caller partial pointers), copy its
+    # outputs back -- copies in both directions and the kernel overlap.
+    nch = max(1, args.e2e_chunks)
+    bounds = [(T * c // nch, T * (c + 1) // nch) for c in range(nch)]
+    s_in = torch.cuda.Stream(dev)
+    s_out = torch.cuda.Stream(dev)
+
     def e2e_step():
-        Pd.copy_(Ph, non_blocking=True)
-        Xd.copy_(Xh, non_blocking=True)
-        B.ar_fusion_run(ws, [Pd[r] for r in range(R)], Xd, G, w.eps, pattern, residual_out=res,
-                        quant_out=q, scale_out=sf, scale_factor=gs, stream=stream)
-        res_h.copy_(res, non_blocking=True)
-        q_h.copy_(q, non_blocking=True)
-        sf_h.copy_(sf, non_blocking=True)
+        s_in.wait_stream(stream)                   # previous step's kernels done with Pd / Xd
+        s_out.wait_stream(stream)
+        for b0, b1 in bounds:
+            with torch.cuda.stream(s_in):
+                for r in range(R):
+                    Pd[r, b0:b1].copy_(Ph[r, b0:b1], non_blocking=True)
+                Xd[b0:b1].copy_(Xh[b0:b1], non_blocking=True)
+            stream.wait_stream(s_in)
+            B.ar_fusion_run(ws, [Pd[r, b0:b1] for r in range(R)], Xd[b0:b1], G, w.eps, pattern,
+                            residual_out=res[b0:b1], quant_out=q[b0:b1], scale_out=sf[b0:b1],
+                            scale_factor=gs, stream=stream)
+            s_out.wait_stream(stream)
+            with torch.cuda.stream(s_out):
+                res_h[b0:b1].copy_(res[b0:b1], non_blocking=True)
+                q_h[b0:b1].copy_(q[b0:b1], non_blocking=True)
+                sf_h[b0:b1].copy_(sf[b0:b1], non_blocking=True)
+        stream.wait_stream(s_out)                  # the step ends when its outputs are on the host
 
     if e2e_steps:
         e2e_step()
@@ -539,7 +560,8 @@ def main():
                      "algorithmic_bytes_per_launch": bytes_alg,
                      "avg_launch_us": avg_launch_s * 1e6},
         "e2e": ({"value": e2e_value, "unit": "tokens/s",
-                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h} if e2e_steps else None),
+                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                 "pipeline": f"{nch} row chunks, H2D / compute / D2H streams"} if e2e_steps else None),
         "gpu_launches": args.steps,
         "clocks": clk,
     }
