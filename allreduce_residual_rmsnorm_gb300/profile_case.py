@@ -85,6 +85,8 @@ def main(argv=None):
             B.ar_fusion_workspace_stage(ws, r, P[r], mode=mode)
 
     stage()
+    B.ar_fusion_run(ws, None, X, G, w.eps, pat, res, nrm, q, sf, sc)   # untimed: module load
+    torch.cuda.synchronize()
     total = 0.0
     for _ in range(a.iters):
         if a.lamport:
