@@ -323,8 +323,10 @@ int pick_variant(const ar_fusion_ws* ws, const FusedArgs& a)
     if (v != AR_VARIANT_AUTO)
         return v;
     // measured at R = 8, T = 8192, H = 7168: one-row-per-block with one
-    // vector per thread (209.5 us) beats the bulk-copy pipeline (216.8 us)
-    return a.H <= 1024 ? AR_VARIANT_WARP_ROW : AR_VARIANT_CTA_ROW;
+    // vector per thread beats the bulk-copy pipeline (184-188 us vs 210 us);
+    // one row per warp only up to hidden 512 (at hidden 1024 the block
+    // version is faster: 131.5 vs 156.5 us at 32768 tokens)
+    return a.H <= 512 ? AR_VARIANT_WARP_ROW : AR_VARIANT_CTA_ROW;
 }
 
 int launch_fused(ar_fusion_ws* ws, const FusedArgs& a, cudaStream_t s)
@@ -654,7 +656,7 @@ int ar_fusion_norm_amax(ar_fusion_ws* ws, const void* const* partials, int nrank
         return AR_OK;
     a.amax_out = amax_out;
     const LaunchCfg c{ws->sms, s};
-    const int variant = a.H <= 1024 ? AR_VARIANT_WARP_ROW : AR_VARIANT_CTA_ROW;
+    const int variant = a.H <= 512 ? AR_VARIANT_WARP_ROW : AR_VARIANT_CTA_ROW;
     e = launch_fused_rows(ws->dtype, variant, a, c);
     if (e != cudaSuccess)
         return cuda_fail(e, "amax kernel launch");

@@ -234,7 +234,7 @@ int ar_fusion_run_noalloc(const void* const* partials, int nranks, int tokens, i
     if (e != cudaSuccess)
         return nfail(AR_ERR_CUDA, "stage launch: %s", cudaGetErrorString(e));
     const arf::LaunchCfg c{sms, s};
-    e = arf::launch_fused_rows(dtype, hidden_dim <= 1024 ? AR_VARIANT_WARP_ROW : AR_VARIANT_CTA_ROW,
+    e = arf::launch_fused_rows(dtype, hidden_dim <= 512 ? AR_VARIANT_WARP_ROW : AR_VARIANT_CTA_ROW,
                                a, c);
     if (e != cudaSuccess)
         return nfail(AR_ERR_CUDA, "fused kernel launch: %s", cudaGetErrorString(e));
