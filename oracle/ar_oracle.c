@@ -401,6 +401,102 @@ void oracle_sum(int dtype, int acc, int R, int64_t n, int64_t rank_stride, const
         out[i] = rnd_d(dtype, rank_sum(dtype, acc, in + i, rank_stride, R));
 }
 
+/* ------------------------------------------- fp32 element type (f32) --- */
+
+/* The same operation with 32-bit float elements (FlashInfer workspace
+ * creation's use_fp32_lamport: the exchanged buffers hold fp32).  Every
+ * rounding to the element type of the 16-bit path is the identity here:
+ *   s = P_0 + ... + P_{R-1} (fp32, rank order);  y = s + X   -> residual_out
+ *   ss = sum_h y_h^2 in fp64 (exact: 24-bit significands square into 48 bits),
+ *        rounded once to fp32;  rstd = 1 / sqrt(ss / H + eps)
+ *   n = (y * rstd) * gamma                                    -> norm_out
+ * Arrays as in oracle_fused_rows, of float. */
+void oracle_fused_rows_f32(int R, int64_t T, int64_t H, int64_t rank_stride,
+                           const float* partials, const float* residual_in, const float* gamma,
+                           float eps, int64_t row_begin, int64_t row_end, float* residual_out,
+                           float* norm_out, float* rstd_out)
+{
+    (void)T;
+    for (int64_t t = row_begin; t < row_end; ++t) {
+        double ss = 0.0;
+        for (int64_t h = 0; h < H; ++h) {
+            float s = partials[t * H + h];
+            for (int r = 1; r < R; ++r)
+                s = s + partials[(int64_t)r * rank_stride + t * H + h];
+            float y = s + residual_in[t * H + h];
+            if (residual_out)
+                residual_out[t * H + h] = y;
+            ss += (double)y * (double)y;
+        }
+        float ss32 = (float)ss;
+        float ms = ss32 / (float)H;
+        float v = ms + eps;
+        float rstd = 1.0f / sqrtf(v);
+        if (rstd_out)
+            rstd_out[t] = rstd;
+        if (!norm_out)
+            continue;
+        for (int64_t h = 0; h < H; ++h) {
+            float s = partials[t * H + h];
+            for (int r = 1; r < R; ++r)
+                s = s + partials[(int64_t)r * rank_stride + t * H + h];
+            float y = s + residual_in[t * H + h];
+            float ny = y * rstd;
+            norm_out[t * H + h] = ny * gamma[h];
+        }
+    }
+}
+
+float oracle_amax_f32(const float* x, int64_t n)
+{
+    float m = 0.0f;
+    for (int64_t i = 0; i < n; ++i)
+        m = fmaxf(m, fabsf(x[i]));
+    return m;
+}
+
+void oracle_quant_fp8_f32(const float* n_in, int64_t n, float inv_scale, uint8_t* q)
+{
+    for (int64_t i = 0; i < n; ++i)
+        q[i] = oracle_f32_to_e4m3(n_in[i] * inv_scale);
+}
+
+/* NVFP4 of fp32 values, same block rule as oracle_quant_nvfp4. */
+void oracle_quant_nvfp4_f32(const float* n_in, int64_t T, int64_t H, float gs, uint8_t* quant_out,
+                            uint8_t* scale_out)
+{
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t b = 0; b < H / 16; ++b) {
+            const float* blk = n_in + t * H + b * 16;
+            float bmax = 0.0f;
+            for (int i = 0; i < 16; ++i)
+                bmax = fmaxf(bmax, fabsf(blk[i]));
+            float per_block = bmax / 6.0f;
+            uint8_t sf = oracle_f32_to_e4m3(gs * per_block);
+            scale_out[t * (H / 16) + b] = sf;
+            float dec = oracle_e4m3_to_f32(sf);
+            float enc = (dec == 0.0f) ? 0.0f : gs / dec;
+            for (int k = 0; k < 8; ++k) {
+                uint8_t lo = oracle_f32_to_e2m1(blk[2 * k] * enc);
+                uint8_t hi = oracle_f32_to_e2m1(blk[2 * k + 1] * enc);
+                quant_out[t * (H / 2) + b * 8 + k] = (uint8_t)(lo | (hi << 4));
+            }
+        }
+    }
+}
+
+/* out_i = in_0[i] + ... + in_{R-1}[i] in fp32, rank order. */
+void oracle_sum_f32(int R, int64_t rank_stride, const float* in, float* out, int64_t i_begin,
+                    int64_t i_end)
+{
+    for (int64_t i = i_begin; i < i_end; ++i) {
+        float s = in[i];
+        for (int r = 1; r < R; ++r)
+            s = s + in[(int64_t)r * rank_stride + i];
+        out[i] = s;
+    }
+}
+
 /* ------------------------------------------------ workspace arithmetic --- */
 
 /*

@@ -24,7 +24,8 @@ __all__ = [
     "e4m3_encode", "e4m3_decode", "e2m1_encode", "e2m1_decode",
     "lamport_flip", "fused", "amax", "fp8_inv_scale", "quant_fp8",
     "nvfp4_global_scale", "quant_nvfp4", "vector_sum", "workspace_sizes",
-    "lamport_step", "host_threads", "swizzle_scales",
+    "lamport_step", "host_threads", "swizzle_scales", "fused_f32", "amax_f32",
+    "quant_fp8_f32", "quant_nvfp4_f32", "vector_sum_f32",
 ]
 
 BF16 = 0
@@ -102,6 +103,21 @@ def load_library(path: str) -> ctypes.CDLL:
     L.oracle_lamport_step.argtypes = [_i64p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64]
     L.oracle_swizzle_scales.argtypes = [_u8p, ctypes.c_int64, ctypes.c_int64, _u8p]
     L.oracle_swizzle_scales.restype = None
+    L.oracle_fused_rows_f32.argtypes = [
+        ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, _f32p, _f32p, _f32p,
+        ctypes.c_float, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_void_p]
+    L.oracle_fused_rows_f32.restype = None
+    L.oracle_amax_f32.argtypes = [_f32p, ctypes.c_int64]
+    L.oracle_amax_f32.restype = ctypes.c_float
+    L.oracle_quant_fp8_f32.argtypes = [_f32p, ctypes.c_int64, ctypes.c_float, _u8p]
+    L.oracle_quant_fp8_f32.restype = None
+    L.oracle_quant_nvfp4_f32.argtypes = [_f32p, ctypes.c_int64, ctypes.c_int64, ctypes.c_float,
+                                         _u8p, _u8p]
+    L.oracle_quant_nvfp4_f32.restype = None
+    L.oracle_sum_f32.argtypes = [ctypes.c_int, ctypes.c_int64, _f32p, ctypes.c_void_p,
+                                 ctypes.c_int64, ctypes.c_int64]
+    L.oracle_sum_f32.restype = None
     L.oracle_lamport_step.restype = None
     return L
 
@@ -291,4 +307,62 @@ def swizzle_scales(linear: np.ndarray) -> np.ndarray:
     T, KB = linear.shape
     out = np.zeros((T + 127) // 128 * 128 * ((KB + 3) // 4) * 4, np.uint8)
     lib().oracle_swizzle_scales(linear, T, KB, out)
+    return out
+
+
+# ------------------------------------------------------ fp32 element type --
+
+def fused_f32(partials, residual_in, gamma, eps, threads: int | None = None):
+    """fp32 elements: partials float32 [R, T, H] -> (residual_out, norm_out,
+    rstd) float32."""
+    partials = np.ascontiguousarray(partials, dtype=np.float32)
+    residual_in = np.ascontiguousarray(residual_in, dtype=np.float32)
+    gamma = np.ascontiguousarray(gamma, dtype=np.float32)
+    R, T, H = partials.shape
+    res = np.zeros((T, H), np.float32)
+    nrm = np.zeros((T, H), np.float32)
+    rstd = np.zeros(T, np.float32)
+    L = lib()
+
+    def run(rb, re_):
+        L.oracle_fused_rows_f32(R, T, H, T * H, partials, residual_in, gamma, ctypes.c_float(eps),
+                                rb, re_, res.ctypes.data, nrm.ctypes.data, rstd.ctypes.data)
+
+    nt = threads or host_threads()
+    spans = _chunks(T, nt * 4)
+    if nt > 1 and len(spans) > 1:
+        with ThreadPoolExecutor(nt) as ex:
+            list(ex.map(lambda s: run(*s), spans))
+    else:
+        for s in spans:
+            run(*s)
+    return res, nrm, rstd
+
+
+def amax_f32(x) -> float:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    return float(lib().oracle_amax_f32(x.reshape(-1), x.size))
+
+
+def quant_fp8_f32(n, inv_scale):
+    n = np.ascontiguousarray(n, dtype=np.float32)
+    q = np.zeros(n.shape, np.uint8)
+    lib().oracle_quant_fp8_f32(n.reshape(-1), n.size, ctypes.c_float(inv_scale), q.reshape(-1))
+    return q
+
+
+def quant_nvfp4_f32(n, gs):
+    n = np.ascontiguousarray(n, dtype=np.float32)
+    T, H = n.shape
+    q = np.zeros((T, H // 2), np.uint8)
+    s = np.zeros((T, H // 16), np.uint8)
+    lib().oracle_quant_nvfp4_f32(n, T, H, ctypes.c_float(gs), q, s)
+    return q, s
+
+
+def vector_sum_f32(ins) -> np.ndarray:
+    ins = np.ascontiguousarray(ins, dtype=np.float32)
+    R, N = ins.shape
+    out = np.zeros(N, np.float32)
+    lib().oracle_sum_f32(R, N, ins, out.ctypes.data, 0, N)
     return out

@@ -418,3 +418,94 @@ def test_swizzled_scales_worked_positions():
     ids[0, 0], ids[1, 0], ids[32, 0], ids[96, 3], ids[31, 2], ids[0, 4] = 1, 2, 3, 4, 5, 6
     out = oracle.swizzle_scales(ids)
     assert (out[0], out[16], out[4], out[15], out[31 * 16 + 2], out[512]) == (1, 2, 3, 4, 5, 6)
+
+
+# ------------------------------------------------------ fp32 element type
+
+def run32(partials, residual, gamma, eps):
+    return oracle.fused_f32(partials.numpy(), residual.numpy(), gamma.numpy(), eps, threads=2)
+
+
+@pytest.mark.parametrize("R", [1, 2, 4, 8, 16])
+def test_f32_identical_partials_power_of_two_ranks(R):
+    # k * x is exact in fp32 for k <= R (powers of two and small multiples of
+    # a value with a short significand): x drawn with 16 significant bits
+    g = torch.Generator().manual_seed(R)
+    x = (torch.randn(4, 64, generator=g) * 1024).round() / 1024
+    res = torch.randn(4, 64, generator=g)
+    gamma = 1 + 0.1 * torch.randn(64, generator=g)
+    out, _, _ = run32(x.unsqueeze(0).expand(R, 4, 64).contiguous(), res, gamma, 1e-6)
+    assert np.array_equal(out, (x * R + res).numpy())        # torch fp32: one rounding
+
+
+def test_f32_zero_partials_and_textbook_rmsnorm():
+    g = torch.Generator().manual_seed(8)
+    res = torch.randn(6, 512, generator=g)
+    gamma = 1 + 0.1 * torch.randn(512, generator=g)
+    out, nrm, _ = run32(torch.zeros(3, 6, 512), res, gamma, 1e-5)
+    assert np.array_equal(out, res.numpy())
+    ref = F.rms_norm(res.double(), (512,), gamma.double(), 1e-5).float().numpy()
+    assert np.allclose(nrm, ref, rtol=2e-6, atol=1e-7)
+
+
+def test_f32_rank_order_worked_value():
+    P = torch.zeros(3, 1, 8)
+    P[0], P[1], P[2] = 2.0 ** 24, 1.0, -(2.0 ** 24)
+    out, _, _ = run32(P, torch.full((1, 8), 0.5), torch.ones(8), 1e-6)
+    assert np.all(out == np.float32(0.5))                    # (2^24 + 1) rounds to 2^24
+
+
+def test_f32_constant_power_of_two_row():
+    g = torch.Generator().manual_seed(9)
+    gamma = 1 + 0.3 * torch.randn(4096, generator=g)
+    _, nrm, rstd = run32(torch.zeros(2, 1, 4096), torch.full((1, 4096), -0.125), gamma, 0.0)
+    assert rstd[0] == np.float32(8.0)
+    assert np.array_equal(nrm[0], (-gamma).numpy())
+
+
+def test_f32_quantisers_match_the_16_bit_ones_on_representable_values():
+    # n values that are exact bf16 numbers give the same codes through the
+    # fp32 and the bf16 entry points
+    g = torch.Generator().manual_seed(10)
+    n16 = (torch.randn(8, 256, generator=g) * 3).to(torch.bfloat16)
+    n32 = n16.float().numpy()
+    assert np.array_equal(oracle.quant_fp8_f32(n32, 17.5), oracle.quant_fp8(BF16, bits(n16), 17.5))
+    q32, s32 = oracle.quant_nvfp4_f32(n32, 300.0)
+    q16, s16 = oracle.quant_nvfp4(BF16, bits(n16), 300.0)
+    assert np.array_equal(q32, q16) and np.array_equal(s32, s16)
+    assert oracle.amax_f32(n32) == oracle.amax(BF16, bits(n16))
+    # the largest magnitude may sit on the negative side
+    assert oracle.amax_f32(np.array([[0.5, -3.5, 2.0, -0.0]], np.float32)) == 3.5
+
+
+def test_f32_vector_sum():
+    x = torch.full((8, 1001), 0.125)
+    assert np.all(oracle.vector_sum_f32(x.numpy()) == 1.0)
+    g = torch.Generator().manual_seed(4)
+    y = torch.rand(4, 999, generator=g) * 2 - 1
+    ref = ((y[0] + y[1]) + y[2]) + y[3]                      # torch fp32, rank order
+    assert np.array_equal(oracle.vector_sum_f32(y.numpy()), ref.numpy())
+
+
+def test_f32_constant_row_with_eps_closed_form():
+    # y = 0.75 everywhere, eps = 0.4375: mean square + eps = 1 exactly, so
+    # rstd = 1 and norm_out = 0.75 * gamma exactly
+    g = torch.Generator().manual_seed(12)
+    gamma = 1 + 0.2 * torch.randn(1024, generator=g)
+    P = torch.zeros(4, 3, 1024)
+    P[1] = 0.5
+    out, nrm, rstd = run32(P, torch.full((3, 1024), 0.25), gamma, 0.4375)
+    assert np.all(out == np.float32(0.75)) and np.all(rstd == np.float32(1.0))
+    assert np.array_equal(nrm, (0.75 * gamma).expand(3, 1024).numpy())
+
+
+def test_f32_norm_is_rmsnorm_of_residual_out():
+    # with nonzero partials the normalised row is the textbook RMSNorm of the
+    # updated residual (computed here in fp64 by torch)
+    g = torch.Generator().manual_seed(13)
+    P = torch.randn(4, 5, 768, generator=g)
+    res = torch.randn(5, 768, generator=g)
+    gamma = 1 + 0.1 * torch.randn(768, generator=g)
+    out, nrm, _ = run32(P, res, gamma, 1e-6)
+    ref = F.rms_norm(torch.from_numpy(out).double(), (768,), gamma.double(), 1e-6).float().numpy()
+    assert np.allclose(nrm, ref, rtol=2e-6, atol=1e-7)

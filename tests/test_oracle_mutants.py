@@ -29,10 +29,10 @@ MUTANTS = {
                       "    double s = dec_d(dtype, p[0]);\n    for (int r = 1; r < R; ++r) {\n        s = s + dec_d(dtype, p[(int64_t)r * stride]);\n        if (acc)\n            s = dec_d(dtype, rnd_d(dtype, (float)s));\n    }\n    return (float)s;"),
     "acc_rounding_dropped": ("        if (acc)\n            s = dec_d(dtype, rnd_d(dtype, s));", "        if (0)\n            s = dec_d(dtype, rnd_d(dtype, s));"),
     "acc_rounding_always": ("        if (acc)\n            s = dec_d(dtype, rnd_d(dtype, s));", "        if (1)\n            s = dec_d(dtype, rnd_d(dtype, s));"),
-    "mean_over_H_minus_1": ("float ms = ss32 / (float)H;", "float ms = ss32 / (float)(H - 1);"),
-    "eps_dropped": ("float v = ms + eps;", "float v = ms;"),
+    "mean_over_H_minus_1": ("float ms = ss32 / (float)H;", "float ms = ss32 / (float)(H - 1);", 0),
+    "eps_dropped": ("float v = ms + eps;", "float v = ms;", 0),
     "eps_outside_sqrt": ("float v = ms + eps;\n        float rstd = 1.0f / sqrtf(v);",
-                         "float v = ms;\n        float rstd = 1.0f / (sqrtf(v) + eps);"),
+                         "float v = ms;\n        float rstd = 1.0f / (sqrtf(v) + eps);", 0),
     "gamma_reversed": ("float n = ny * dec_d(dtype, gamma[h]);", "float n = ny * dec_d(dtype, gamma[H - 1 - h]);"),
     "norm_uses_unrounded_sum": ("float ny = dec_d(dtype, y) * rstd;", "float ny = (dec_d(dtype, a) + dec_d(dtype, residual_in[t * H + h])) * rstd;"),
     "bf16_ties_away": ("if (dropped > 0x8000u || (dropped == 0x8000u && (kept & 1u)))",
@@ -46,14 +46,35 @@ MUTANTS = {
     "e2m1_ties_away": ("if (frac > 0.5f || (frac == 0.5f && (n & 1u)))\n        n += 1u;\n    if (ax < 1.0f && n < 2u)",
                        "if (frac >= 0.5f)\n        n += 1u;\n    if (ax < 1.0f && n < 2u)"),
     "e2m1_saturate_low": ("return s | 0x7;\n    int e;", "return s | 0x6;\n    int e;"),
-    "nvfp4_no_div6": ("float per_block = bmax / 6.0f;", "float per_block = bmax;"),
-    "nvfp4_nibbles_swapped": ("(uint8_t)(lo | (hi << 4))", "(uint8_t)(hi | (lo << 4))"),
-    "nvfp4_enc_inverted": ("float enc = (dec == 0.0f) ? 0.0f : gs / dec;", "float enc = (dec == 0.0f) ? 0.0f : dec / gs;"),
+    "nvfp4_no_div6": ("float per_block = bmax / 6.0f;", "float per_block = bmax;", 0),
+    "nvfp4_nibbles_swapped": ("(uint8_t)(lo | (hi << 4))", "(uint8_t)(hi | (lo << 4))", 0),
+    "nvfp4_enc_inverted": ("float enc = (dec == 0.0f) ? 0.0f : gs / dec;", "float enc = (dec == 0.0f) ? 0.0f : dec / gs;", 0),
     "fp8_scale_not_inverted": ("return 1.0f / scale;", "return scale;"),
     "flip_wrong_word": ("if (words[i] == 0x80000000u)", "if (words[i] == 0x00008000u)"),
     "sum_without_rounding": ("out[i] = rnd_d(dtype, rank_sum(dtype, acc, in + i, rank_stride, R));",
                              "out[i] = (uint16_t)rank_sum(dtype, acc, in + i, rank_stride, R);"),
     "lamport_clear_wrong_slot": ("io[3] = (flag + 2) % 3;", "io[3] = (flag + 1) % 3;"),
+    # fp32 element type
+    "f32_drop_residual": ("float y = s + residual_in[t * H + h];\n            if (residual_out)",
+                          "float y = s + 0.0f;\n            if (residual_out)"),
+    "f32_skip_last_rank": ("for (int r = 1; r < R; ++r)\n                s = s + partials[",
+                           "for (int r = 1; r < R - 1; ++r)\n                s = s + partials[", 0),
+    "f32_norm_skips_last_rank": ("for (int r = 1; r < R; ++r)\n                s = s + partials[",
+                                 "for (int r = 1; r < R - 1; ++r)\n                s = s + partials[", 1),
+    "f32_fp64_rank_sum": ("            float s = partials[t * H + h];\n            for (int r = 1; r < R; ++r)",
+                          "            double s = partials[t * H + h];\n            for (int r = 1; r < R; ++r)", 0),
+    "f32_mean_over_H_minus_1": ("float ms = ss32 / (float)H;", "float ms = ss32 / (float)(H - 1);", 1),
+    "f32_eps_dropped": ("float v = ms + eps;", "float v = ms;", 1),
+    "f32_eps_outside_sqrt": ("float v = ms + eps;\n        float rstd = 1.0f / sqrtf(v);",
+                             "float v = ms;\n        float rstd = 1.0f / (sqrtf(v) + eps);", 1),
+    "f32_gamma_reversed": ("norm_out[t * H + h] = ny * gamma[h];", "norm_out[t * H + h] = ny * gamma[H - 1 - h];"),
+    "f32_amax_no_abs": ("m = fmaxf(m, fabsf(x[i]));", "m = fmaxf(m, x[i]);"),
+    "f32_fp8_scale_ignored": ("q[i] = oracle_f32_to_e4m3(n_in[i] * inv_scale);", "q[i] = oracle_f32_to_e4m3(n_in[i]);"),
+    "f32_nvfp4_no_div6": ("float per_block = bmax / 6.0f;", "float per_block = bmax;", 1),
+    "f32_nvfp4_nibbles_swapped": ("(uint8_t)(lo | (hi << 4))", "(uint8_t)(hi | (lo << 4))", 1),
+    "f32_nvfp4_enc_inverted": ("float enc = (dec == 0.0f) ? 0.0f : gs / dec;",
+                               "float enc = (dec == 0.0f) ? 0.0f : dec / gs;", 1),
+    "f32_sum_subtract": ("s = s + in[(int64_t)r * rank_stride + i];", "s = s - in[(int64_t)r * rank_stride + i];"),
     "buffer_size_missing_R": ("out[0] = (int64_t)R * max_tokens * H * elem_bytes;", "out[0] = max_tokens * H * elem_bytes;"),
 }
 
@@ -83,15 +104,34 @@ PINS = [
     Fz.test_vector_sum_element_type_accumulation,
     Fz.test_workspace_sizes_match_page_formula_golden,
     Fz.test_lamport_state_cycles,
+    lambda: [Fz.test_f32_identical_partials_power_of_two_ranks(R) for R in (2, 8)],
+    Fz.test_f32_zero_partials_and_textbook_rmsnorm,
+    Fz.test_f32_rank_order_worked_value,
+    Fz.test_f32_constant_power_of_two_row,
+    Fz.test_f32_constant_row_with_eps_closed_form,
+    Fz.test_f32_norm_is_rmsnorm_of_residual_out,
+    Fz.test_f32_quantisers_match_the_16_bit_ones_on_representable_values,
+    Fz.test_f32_vector_sum,
 ]
 
 
 def _build_mutant(tmp_path, name):
     src = open(SRC).read()
-    old, new = MUTANTS[name]
-    assert src.count(old) == 1, f"mutation anchor for {name} not unique/present"
+    old, new, *which = MUTANTS[name]
+    if which:
+        # the k-th of several identical lines (the 16-bit function comes first,
+        # its fp32 counterpart second)
+        k = which[0]
+        assert src.count(old) > k, f"mutation anchor for {name} has no occurrence {k}"
+        at = -1
+        for _ in range(k + 1):
+            at = src.index(old, at + 1)
+        src = src[:at] + new + src[at + len(old):]
+    else:
+        assert src.count(old) == 1, f"mutation anchor for {name} not unique/present"
+        src = src.replace(old, new)
     path = tmp_path / f"{name}.c"
-    path.write_text(src.replace(old, new))
+    path.write_text(src)
     so = tmp_path / f"{name}.so"
     subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
                            "-fPIC", "-shared", str(path), "-o", str(so), "-lm"])
