@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(HERE, "libarfusion.so")
 # enum ar_dtype
 AR_DT_BF16 = 0
 AR_DT_FP16 = 1
+AR_DT_FP32 = 2
 # enum ar_pattern
 AR_RESIDUAL_OUT = 1
 AR_NORM_OUT = 2
@@ -164,6 +165,8 @@ def _dtype_id(t: torch.Tensor) -> int:
         return AR_DT_BF16
     if t.dtype == torch.float16:
         return AR_DT_FP16
+    if t.dtype == torch.float32:
+        return AR_DT_FP32
     raise TypeError(f"unsupported element type {t.dtype}")
 
 

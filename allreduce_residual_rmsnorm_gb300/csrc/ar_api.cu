@@ -24,11 +24,16 @@
 namespace arf {
 cudaError_t launch_fused_rows_bf16(int variant, const FusedArgs& a, const LaunchCfg& c);
 cudaError_t launch_fused_rows_fp16(int variant, const FusedArgs& a, const LaunchCfg& c);
+cudaError_t launch_fused_rows_fp32(int variant, const FusedArgs& a, const LaunchCfg& c);
 
 cudaError_t launch_fused_rows(int dtype, int variant, const FusedArgs& a, const LaunchCfg& c)
 {
-    return dtype == AR_DT_BF16 ? launch_fused_rows_bf16(variant, a, c)
-                               : launch_fused_rows_fp16(variant, a, c);
+    switch (dtype) {
+    case AR_DT_BF16: return launch_fused_rows_bf16(variant, a, c);
+    case AR_DT_FP16: return launch_fused_rows_fp16(variant, a, c);
+    case AR_DT_FP32: return launch_fused_rows_fp32(variant, a, c);
+    default: return cudaErrorInvalidValue;
+    }
 }
 }  // namespace arf
 
@@ -76,10 +81,10 @@ struct Layout {
         total;
 };
 
-Layout layout_of(int R, int maxT, int H)
+Layout layout_of(int R, int maxT, int H, int dtype)
 {
     Layout L;
-    const uint64_t elem = 2;
+    const uint64_t elem = (uint64_t)elem_bytes(dtype);
     const uint64_t tok = (uint64_t)(maxT > AR_ONESHOT_MAX_TOKENS ? maxT : AR_ONESHOT_MAX_TOKENS);
     L.buffer_off = 0;
     L.buffer_bytes = (uint64_t)R * maxT * H * elem;
@@ -94,8 +99,8 @@ Layout layout_of(int R, int maxT, int H)
 
 int check_shape(int tp_size, int max_token_num, int hidden_dim, int dtype)
 {
-    if (dtype != AR_DT_BF16 && dtype != AR_DT_FP16)
-        return fail(AR_ERR_UNSUPPORTED, "dtype %d is not bf16 (0) or fp16 (1)", dtype);
+    if (!dtype_supported(dtype))
+        return fail(AR_ERR_UNSUPPORTED, "dtype %d is not bf16 (0), fp16 (1) or fp32 (2)", dtype);
     if (tp_size < 1 || tp_size > AR_MAX_RANKS)
         return fail(AR_ERR_UNSUPPORTED, "tp_size %d outside 1..%d", tp_size, AR_MAX_RANKS);
     if (max_token_num < 1)
@@ -220,8 +225,8 @@ int prepare(ar_fusion_ws* ws, const void* const* partials, int nranks, int token
     launch = false;
     if (!ws)
         return fail(AR_ERR_INVALID, "workspace is NULL");
-    if (dtype != AR_DT_BF16 && dtype != AR_DT_FP16)
-        return fail(AR_ERR_UNSUPPORTED, "dtype %d is not bf16 (0) or fp16 (1)", dtype);
+    if (!dtype_supported(dtype))
+        return fail(AR_ERR_UNSUPPORTED, "dtype %d is not bf16 (0), fp16 (1) or fp32 (2)", dtype);
     if (dtype != ws->dtype)
         return fail(AR_ERR_INVALID, "dtype %d differs from the workspace's %d", dtype, ws->dtype);
     if (nranks < 1 || nranks > AR_MAX_RANKS)
@@ -255,16 +260,18 @@ int prepare(ar_fusion_ws* ws, const void* const* partials, int nranks, int token
     if (tokens == 0)
         return AR_OK;
 
-    // pointers
+    // pointers: element arrays aligned for the vector accesses (16 bytes,
+    // 32 for fp32), byte outputs to 16 bytes
+    const auto va = [dtype](const void* p) { return vec_aligned(p, dtype); };
     if (!residual_in || !gamma)
         return fail(AR_ERR_INVALID, "residual_in and gamma must be non-NULL");
-    if (!aligned16(residual_in) || !aligned16(gamma))
-        return fail(AR_ERR_INVALID, "residual_in / gamma not 16-byte aligned");
+    if (!va(residual_in) || !va(gamma))
+        return fail(AR_ERR_INVALID, "residual_in / gamma not vector aligned");
     if (!calib) {
-        if ((pattern & AR_RESIDUAL_OUT) && (!residual_out || !aligned16(residual_out)))
-            return fail(AR_ERR_INVALID, "residual_out NULL or not 16-byte aligned");
-        if ((pattern & AR_NORM_OUT) && (!norm_out || !aligned16(norm_out)))
-            return fail(AR_ERR_INVALID, "norm_out NULL or not 16-byte aligned");
+        if ((pattern & AR_RESIDUAL_OUT) && (!residual_out || !va(residual_out)))
+            return fail(AR_ERR_INVALID, "residual_out NULL or not vector aligned");
+        if ((pattern & AR_NORM_OUT) && (!norm_out || !va(norm_out)))
+            return fail(AR_ERR_INVALID, "norm_out NULL or not vector aligned");
         if (pattern & (AR_QUANT_FP8 | AR_QUANT_NVFP4)) {
             if (!quant_out || !aligned16(quant_out))
                 return fail(AR_ERR_INVALID, "quant_out NULL or not 16-byte aligned");
@@ -278,13 +285,14 @@ int prepare(ar_fusion_ws* ws, const void* const* partials, int nranks, int token
     memset(&a, 0, sizeof a);
     if (!staged) {
         for (int r = 0; r < nranks; ++r) {
-            if (!partials[r] || !aligned16(partials[r]))
-                return fail(AR_ERR_INVALID, "partials[%d] NULL or not 16-byte aligned", r);
+            if (!partials[r] || !va(partials[r]))
+                return fail(AR_ERR_INVALID, "partials[%d] NULL or not vector aligned", r);
             a.partial[r] = static_cast<const uint8_t*>(partials[r]);
         }
     } else if (mode == AR_MODE_BUFFER) {
         for (int r = 0; r < nranks; ++r)
-            a.partial[r] = ws->base + ws->buffer_off + (uint64_t)r * ws->maxT * ws->H * 2;
+            a.partial[r] = ws->base + ws->buffer_off +
+                           (uint64_t)r * ws->maxT * ws->H * elem_bytes(ws->dtype);
     } else {
         a.lamport = 1;
         a.lamport_base = ws->base + ws->lamport_off;
@@ -367,7 +375,7 @@ int ar_fusion_workspace_bytes(int tp_size, int max_token_num, int hidden_dim, in
     int rc = check_shape(tp_size, max_token_num, hidden_dim, dtype);
     if (rc)
         return rc;
-    *bytes = (size_t)layout_of(tp_size, max_token_num, hidden_dim).total;
+    *bytes = (size_t)layout_of(tp_size, max_token_num, hidden_dim, dtype).total;
     return AR_OK;
 }
 
@@ -381,7 +389,7 @@ int ar_fusion_workspace_create(int tp_size, int max_token_num, int hidden_dim, i
     int rc = check_shape(tp_size, max_token_num, hidden_dim, dtype);
     if (rc)
         return rc;
-    const Layout L = layout_of(tp_size, max_token_num, hidden_dim);
+    const Layout L = layout_of(tp_size, max_token_num, hidden_dim, dtype);
     if (device_mem && (device_mem_bytes < L.total || ((uintptr_t)device_mem & 255)))
         return fail(AR_ERR_INVALID, "device_mem too small (%zu < %llu) or not 256-byte aligned",
                     device_mem_bytes, (unsigned long long)L.total);
@@ -473,7 +481,7 @@ int ar_fusion_workspace_info(const ar_fusion_ws* ws, ar_fusion_ws_info* info)
     info->max_token_num = ws->maxT;
     info->hidden_dim = ws->H;
     info->dtype = ws->dtype;
-    info->elem_bytes = 2;
+    info->elem_bytes = elem_bytes(ws->dtype);
     info->oneshot_max_tokens = AR_ONESHOT_MAX_TOKENS;
     info->total_bytes = ws->total;
     info->buffer_bytes = ws->buffer_bytes;
@@ -600,10 +608,11 @@ int ar_fusion_workspace_stage(ar_fusion_ws* ws, int rank, const void* src, int t
         return fail(AR_ERR_CAPACITY, "tokens %d > max_token_num %d", tokens, ws->maxT);
     if (tokens == 0)
         return AR_OK;
-    if (!src || !aligned16(src))
-        return fail(AR_ERR_INVALID, "src NULL or not 16-byte aligned");
+    if (!src || !vec_aligned(src, ws->dtype))
+        return fail(AR_ERR_INVALID, "src NULL or not vector aligned");
     mode = resolve_mode(ws, mode, tokens);
-    const uint64_t plane = (uint64_t)tokens * ws->H * 2;
+    const uint64_t eb = (uint64_t)elem_bytes(ws->dtype);
+    const uint64_t plane = (uint64_t)tokens * ws->H * eb;
     const uint64_t nvec = plane / 16;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (mode == AR_MODE_LAMPORT) {
@@ -613,7 +622,7 @@ int ar_fusion_workspace_stage(ar_fusion_ws* ws, int rank, const void* src, int t
     } else {
         stage_kernel<<<grid_for(nvec, 256, ws->sms), 256, 0, s>>>(
             static_cast<const uint4*>(src), ws->base + ws->buffer_off, 0,
-            (uint64_t)rank * ws->maxT * ws->H * 2, nvec, 0, state_of(ws));
+            (uint64_t)rank * ws->maxT * ws->H * eb, nvec, 0, state_of(ws));
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
@@ -674,18 +683,19 @@ int ar_fusion_sum_ex(const void* const* bufs, int nranks, size_t n, int dtype, i
 {
     if (accumulate != AR_ACC_FP32 && accumulate != AR_ACC_ELEMENT)
         return fail(AR_ERR_INVALID, "accumulate %d unknown", accumulate);
-    if (dtype != AR_DT_BF16 && dtype != AR_DT_FP16)
-        return fail(AR_ERR_UNSUPPORTED, "dtype %d is not bf16 (0) or fp16 (1)", dtype);
+    if (!dtype_supported(dtype))
+        return fail(AR_ERR_UNSUPPORTED, "dtype %d is not bf16 (0), fp16 (1) or fp32 (2)", dtype);
     if (nranks < 1 || nranks > AR_MAX_RANKS)
         return fail(AR_ERR_UNSUPPORTED, "nranks %d outside 1..%d", nranks, AR_MAX_RANKS);
     if (n == 0)
         return AR_OK;
-    if (!bufs || !out || ((uintptr_t)out & 1))
+    const uintptr_t emask = (uintptr_t)elem_bytes(dtype) - 1;
+    if (!bufs || !out || ((uintptr_t)out & emask))
         return fail(AR_ERR_INVALID, "bufs / out NULL or out misaligned");
     SumArgs a;
     memset(&a, 0, sizeof a);
     for (int r = 0; r < nranks; ++r) {
-        if (!bufs[r] || ((uintptr_t)bufs[r] & 1))
+        if (!bufs[r] || ((uintptr_t)bufs[r] & emask))
             return fail(AR_ERR_INVALID, "bufs[%d] NULL or misaligned", r);
         a.in[r] = static_cast<const uint8_t*>(bufs[r]);
     }

@@ -14,11 +14,26 @@
 
 namespace arf {
 
+// A "vector" is 8 consecutive elements of a row: 16 bytes of bf16 / fp16
+// (one uint4) or 32 bytes of fp32 (one V32, moved by a single 256-bit access).
+struct V32 {
+    uint4 lo, hi;
+};
+
 struct Bf16 {
     static constexpr int id = AR_DT_BF16;
+    static constexpr int bytes = 2;
+    using Vec = uint4;
 };
 struct Fp16 {
     static constexpr int id = AR_DT_FP16;
+    static constexpr int bytes = 2;
+    using Vec = uint4;
+};
+struct F32 {
+    static constexpr int id = AR_DT_FP32;
+    static constexpr int bytes = 4;
+    using Vec = V32;
 };
 
 // ------------------------------------------------------ 16-bit element pairs
@@ -64,25 +79,41 @@ __device__ __forceinline__ uint32_t pack2<Fp16>(float lo, float hi)
     return w;
 }
 
-// 8 elements of a 16-byte vector -> fp32
+// 8 elements of a vector -> fp32 (exact)
 template <class D>
-__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8])
+__device__ __forceinline__ void unpack8(const typename D::Vec& v, float (&f)[8])
 {
-    float2 p;
-    p = unpack2<D>(v.x); f[0] = p.x; f[1] = p.y;
-    p = unpack2<D>(v.y); f[2] = p.x; f[3] = p.y;
-    p = unpack2<D>(v.z); f[4] = p.x; f[5] = p.y;
-    p = unpack2<D>(v.w); f[6] = p.x; f[7] = p.y;
+    if constexpr (D::bytes == 4) {
+        f[0] = __uint_as_float(v.lo.x); f[1] = __uint_as_float(v.lo.y);
+        f[2] = __uint_as_float(v.lo.z); f[3] = __uint_as_float(v.lo.w);
+        f[4] = __uint_as_float(v.hi.x); f[5] = __uint_as_float(v.hi.y);
+        f[6] = __uint_as_float(v.hi.z); f[7] = __uint_as_float(v.hi.w);
+    } else {
+        float2 p;
+        p = unpack2<D>(v.x); f[0] = p.x; f[1] = p.y;
+        p = unpack2<D>(v.y); f[2] = p.x; f[3] = p.y;
+        p = unpack2<D>(v.z); f[4] = p.x; f[5] = p.y;
+        p = unpack2<D>(v.w); f[6] = p.x; f[7] = p.y;
+    }
 }
 
+// 8 fp32 -> a vector, each rounded to the element type (nearest even; the
+// identity for fp32)
 template <class D>
-__device__ __forceinline__ uint4 pack8(const float (&f)[8])
+__device__ __forceinline__ typename D::Vec pack8(const float (&f)[8])
 {
-    uint4 v;
-    v.x = pack2<D>(f[0], f[1]);
-    v.y = pack2<D>(f[2], f[3]);
-    v.z = pack2<D>(f[4], f[5]);
-    v.w = pack2<D>(f[6], f[7]);
+    typename D::Vec v;
+    if constexpr (D::bytes == 4) {
+        v.lo = make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                          __float_as_uint(f[3]));
+        v.hi = make_uint4(__float_as_uint(f[4]), __float_as_uint(f[5]), __float_as_uint(f[6]),
+                          __float_as_uint(f[7]));
+    } else {
+        v.x = pack2<D>(f[0], f[1]);
+        v.y = pack2<D>(f[2], f[3]);
+        v.z = pack2<D>(f[4], f[5]);
+        v.w = pack2<D>(f[6], f[7]);
+    }
     return v;
 }
 
@@ -115,19 +146,29 @@ __device__ __forceinline__ void add2<Fp16>(float& lo, float& hi, uint32_t w)
 
 // s[i] = s[i] + f(v_i), i < 8
 template <class D>
-__device__ __forceinline__ void add8(float (&s)[8], const uint4& v)
+__device__ __forceinline__ void add8(float (&s)[8], const typename D::Vec& v)
 {
-    add2<D>(s[0], s[1], v.x);
-    add2<D>(s[2], s[3], v.y);
-    add2<D>(s[4], s[5], v.z);
-    add2<D>(s[6], s[7], v.w);
+    if constexpr (D::bytes == 4) {
+        float t[8];
+        unpack8<D>(v, t);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            s[i] = __fadd_rn(s[i], t[i]);
+    } else {
+        add2<D>(s[0], s[1], v.x);
+        add2<D>(s[2], s[3], v.y);
+        add2<D>(s[4], s[5], v.z);
+        add2<D>(s[6], s[7], v.w);
+    }
 }
 
 // s[i] = f(rnd(s[i])): the element-type accumulation rounds every partial sum
+// (nothing to do for fp32 elements)
 template <class D>
 __device__ __forceinline__ void round8(float (&s)[8])
 {
-    unpack8<D>(pack8<D>(s), s);
+    if constexpr (D::bytes != 4)
+        unpack8<D>(pack8<D>(s), s);
 }
 
 // Squares of a packed pair, exact (8- or 11-bit significands): fma with a
@@ -193,6 +234,82 @@ __device__ __forceinline__ void st_vec(void* p, const uint4& v)
     *reinterpret_cast<uint4*>(p) = v;
 }
 
+// 256-bit forms for 8 fp32 elements (32-byte aligned addresses)
+__device__ __forceinline__ V32 ld_stream32(const void* p)
+{
+    V32 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v.lo.x), "=r"(v.lo.y), "=r"(v.lo.z), "=r"(v.lo.w), "=r"(v.hi.x),
+                   "=r"(v.hi.y), "=r"(v.hi.z), "=r"(v.hi.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ V32 ld_poll32(const void* p)
+{
+    V32 v;
+    asm volatile("ld.volatile.global.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v.lo.x), "=r"(v.lo.y), "=r"(v.lo.z), "=r"(v.lo.w), "=r"(v.hi.x),
+                   "=r"(v.hi.y), "=r"(v.hi.z), "=r"(v.hi.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ V32 ld_keep32(const void* p)
+{
+    V32 v;
+    asm("ld.global.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=r"(v.lo.x), "=r"(v.lo.y), "=r"(v.lo.z), "=r"(v.lo.w), "=r"(v.hi.x), "=r"(v.hi.y),
+          "=r"(v.hi.z), "=r"(v.hi.w)
+        : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_vec(void* p, const V32& v)
+{
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v.lo.x),
+                 "r"(v.lo.y), "r"(v.lo.z), "r"(v.lo.w), "r"(v.hi.x), "r"(v.hi.y), "r"(v.hi.z),
+                 "r"(v.hi.w)
+                 : "memory");
+}
+
+// Vector loads by element type: streaming (read once), polling (volatile),
+// cached (gamma)
+template <class D>
+__device__ __forceinline__ typename D::Vec ld_stream_v(const void* p)
+{
+    if constexpr (D::bytes == 4)
+        return ld_stream32(p);
+    else
+        return ld_stream(p);
+}
+
+template <class D>
+__device__ __forceinline__ typename D::Vec ld_poll_v(const void* p)
+{
+    if constexpr (D::bytes == 4)
+        return ld_poll32(p);
+    else
+        return ld_poll(p);
+}
+
+template <class D>
+__device__ __forceinline__ typename D::Vec ld_keep_v(const void* p)
+{
+    if constexpr (D::bytes == 4)
+        return ld_keep32(p);
+    else
+        return ld_keep(p);
+}
+
+template <class V>
+__device__ __forceinline__ V zero_vec()
+{
+    V v;
+    memset(&v, 0, sizeof v);
+    return v;
+}
+
 __device__ __forceinline__ void st_u2(void* p, uint32_t a, uint32_t b)
 {
     *reinterpret_cast<uint2*>(p) = make_uint2(a, b);
@@ -204,6 +321,11 @@ __device__ __forceinline__ bool has_sentinel(const uint4& v)
 {
     return (v.x == 0x80000000u) | (v.y == 0x80000000u) | (v.z == 0x80000000u) |
            (v.w == 0x80000000u);
+}
+
+__device__ __forceinline__ bool has_sentinel(const V32& v)
+{
+    return has_sentinel(v.lo) | has_sentinel(v.hi);
 }
 
 __device__ __forceinline__ uint64_t globaltimer_ns()

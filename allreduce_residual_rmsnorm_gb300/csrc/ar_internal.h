@@ -53,6 +53,18 @@ struct SumArgs {
 };
 cudaError_t launch_vector_sum(int dtype, const SumArgs& a, const LaunchCfg& c);
 
+// Element types and the alignment their vector accesses need: 16 bytes for
+// bf16 / fp16 (128-bit), 32 bytes for fp32 (256-bit).
+inline bool dtype_supported(int dtype)
+{
+    return dtype == AR_DT_BF16 || dtype == AR_DT_FP16 || dtype == AR_DT_FP32;
+}
+inline int elem_bytes(int dtype) { return dtype == AR_DT_FP32 ? 4 : 2; }
+inline bool vec_aligned(const void* p, int dtype)
+{
+    return ((uintptr_t)p & (dtype == AR_DT_FP32 ? 31u : 15u)) == 0;
+}
+
 // Record `msg` as the calling thread's ar_fusion_last_error() text; returns code.
 int set_last_error(int code, const char* msg);
 

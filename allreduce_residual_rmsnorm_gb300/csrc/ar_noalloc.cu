@@ -146,8 +146,8 @@ int ar_fusion_run_noalloc(const void* const* partials, int nranks, int tokens, i
                           int pattern, void* residual_out, void* norm_out, void* quant_out,
                           void* scale_out, const float* scale_factor, void* stream)
 {
-    if (dtype != AR_DT_BF16 && dtype != AR_DT_FP16)
-        return nfail(AR_ERR_UNSUPPORTED, "dtype %d is not bf16 (0) or fp16 (1)", dtype);
+    if (!arf::dtype_supported(dtype))
+        return nfail(AR_ERR_UNSUPPORTED, "dtype %d is not bf16 (0), fp16 (1) or fp32 (2)", dtype);
     if (nranks < 1 || nranks > AR_MAX_RANKS)
         return nfail(AR_ERR_UNSUPPORTED, "nranks %d outside 1..%d", nranks, AR_MAX_RANKS);
     if (tokens < 0)
@@ -160,10 +160,10 @@ int ar_fusion_run_noalloc(const void* const* partials, int nranks, int tokens, i
         return nfail(AR_ERR_INVALID, "unsupported pattern 0x%x", pattern);
     if ((pattern & AR_QUANT_NVFP4) && hidden_dim % 16 != 0)
         return nfail(AR_ERR_INVALID, "NVFP4 needs hidden_dim %% 16 == 0 (got %d)", hidden_dim);
-    const uint64_t plane = (uint64_t)tokens * hidden_dim * 2;
+    const uint64_t plane = (uint64_t)tokens * hidden_dim * arf::elem_bytes(dtype);
     if (plane * (uint64_t)nranks > kSlotBytes)
         return nfail(AR_ERR_CAPACITY,
-                     "nranks * tokens * hidden_dim * 2 = %llu bytes exceeds the fixed scratch "
+                     "nranks * tokens * hidden_dim * elem = %llu bytes exceeds the fixed scratch "
                      "slot of %llu bytes",
                      (unsigned long long)(plane * (uint64_t)nranks),
                      (unsigned long long)kSlotBytes);
@@ -171,12 +171,13 @@ int ar_fusion_run_noalloc(const void* const* partials, int nranks, int tokens, i
         return AR_OK;
     if (!partials)
         return nfail(AR_ERR_INVALID, "partials is NULL");
-    if (!residual_in || !gamma || !aligned16(residual_in) || !aligned16(gamma))
-        return nfail(AR_ERR_INVALID, "residual_in / gamma NULL or not 16-byte aligned");
-    if ((pattern & AR_RESIDUAL_OUT) && (!residual_out || !aligned16(residual_out)))
-        return nfail(AR_ERR_INVALID, "residual_out NULL or not 16-byte aligned");
-    if ((pattern & AR_NORM_OUT) && (!norm_out || !aligned16(norm_out)))
-        return nfail(AR_ERR_INVALID, "norm_out NULL or not 16-byte aligned");
+    const auto va = [dtype](const void* p) { return arf::vec_aligned(p, dtype); };
+    if (!residual_in || !gamma || !va(residual_in) || !va(gamma))
+        return nfail(AR_ERR_INVALID, "residual_in / gamma NULL or not vector aligned");
+    if ((pattern & AR_RESIDUAL_OUT) && (!residual_out || !va(residual_out)))
+        return nfail(AR_ERR_INVALID, "residual_out NULL or not vector aligned");
+    if ((pattern & AR_NORM_OUT) && (!norm_out || !va(norm_out)))
+        return nfail(AR_ERR_INVALID, "norm_out NULL or not vector aligned");
     if (pattern & (AR_QUANT_FP8 | AR_QUANT_NVFP4)) {
         if (!quant_out || !aligned16(quant_out))
             return nfail(AR_ERR_INVALID, "quant_out NULL or not 16-byte aligned");
@@ -189,8 +190,8 @@ int ar_fusion_run_noalloc(const void* const* partials, int nranks, int tokens, i
     arf::FusedArgs a;
     memset(&a, 0, sizeof a);
     for (int r = 0; r < nranks; ++r) {
-        if (!partials[r] || !aligned16(partials[r]))
-            return nfail(AR_ERR_INVALID, "partials[%d] NULL or not 16-byte aligned", r);
+        if (!partials[r] || !va(partials[r]))
+            return nfail(AR_ERR_INVALID, "partials[%d] NULL or not vector aligned", r);
         a.partial[r] = static_cast<const uint8_t*>(partials[r]);
     }
     int dev = 0;

@@ -2,7 +2,8 @@
 // (TensorRT-LLM allReduceFusionKernels.cu: add128 / fused_op for the residual,
 // rms_norm for the normalisation, fused_op's quantised output).
 //
-// A "vector" is 8 consecutive elements of a row (16 bytes of bf16/fp16).
+// A "vector" is 8 consecutive elements of a row (16 bytes of bf16 / fp16, 32
+// bytes of fp32).
 #pragma once
 
 #include "ar_common.cuh"
@@ -12,22 +13,35 @@ namespace arf {
 
 // From the fp32 rank sum s of one vector and the residual x:
 //   a = rnd(s);  y = rnd(f(a) + f(x));  ss += y^2 (exact squares, TwoSum).
-// Returns y (packed).
+// Returns y (packed).  fp32 elements: the square of a 24-bit significand
+// needs 48 bits, so it enters the pair as its rounded product plus the exact
+// remainder (TwoProduct by fma).
 template <class D>
-__device__ __forceinline__ uint4 residual_vec(const float (&s)[8], const uint4& x, DF& ss)
+__device__ __forceinline__ typename D::Vec residual_vec(const float (&s)[8],
+                                                        const typename D::Vec& x, DF& ss)
 {
     float a[8];
     unpack8<D>(pack8<D>(s), a);
     add8<D>(a, x);
-    const uint4 y = pack8<D>(a);
-    float t[8];
-    sq2<D>(t[0], t[1], y.x);
-    sq2<D>(t[2], t[3], y.y);
-    sq2<D>(t[4], t[5], y.z);
-    sq2<D>(t[6], t[7], y.w);
+    const typename D::Vec y = pack8<D>(a);
+    if constexpr (D::bytes == 4) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-        df_add_term(ss, t[i]);
+        for (int i = 0; i < 8; ++i) {
+            const float p = __fmul_rn(a[i], a[i]);
+            const float e = __fmaf_rn(a[i], a[i], -p);
+            df_add_term(ss, p);
+            ss.lo = __fadd_rn(ss.lo, e);
+        }
+    } else {
+        float t[8];
+        sq2<D>(t[0], t[1], y.x);
+        sq2<D>(t[2], t[3], y.y);
+        sq2<D>(t[4], t[5], y.z);
+        sq2<D>(t[6], t[7], y.w);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            df_add_term(ss, t[i]);
+    }
     return y;
 }
 
@@ -80,7 +94,7 @@ template <class D>
 __device__ __forceinline__ void load_gamma(const uint8_t* gamma, int v, bool ok, float (&g)[8])
 {
     if (ok) {
-        unpack8<D>(ld_keep(gamma + (size_t)v * 16), g);
+        unpack8<D>(ld_keep_v<D>(gamma + (size_t)v * 8 * D::bytes), g);
     } else {
 #pragma unroll
         for (int i = 0; i < 8; ++i)
@@ -108,7 +122,8 @@ __device__ __forceinline__ size_t sf_offset(int layout, int m, int k, int kblock
 // of lanes past the end of the row.
 template <class D>
 __device__ __forceinline__ void normalize_vec(const FusedArgs& a, int pat, int row, int v, bool ok,
-                                              const uint4& y, const float (&g)[8], float rstd,
+                                              const typename D::Vec& y, const float (&g)[8],
+                                              float rstd,
                                               float qscale, float& amax_local)
 {
     const int H = a.H;
@@ -117,9 +132,9 @@ __device__ __forceinline__ void normalize_vec(const FusedArgs& a, int pat, int r
 #pragma unroll
     for (int i = 0; i < 8; ++i)
         nf[i] = __fmul_rn(__fmul_rn(yf[i], rstd), g[i]);
-    const uint4 nv = pack8<D>(nf);
+    const typename D::Vec nv = pack8<D>(nf);
     if (ok && (pat & AR_NORM_OUT))
-        st_vec(a.norm_out + ((size_t)row * H + (size_t)v * 8) * 2, nv);
+        st_vec(a.norm_out + ((size_t)row * H + (size_t)v * 8) * D::bytes, nv);
     if (!(pat & (AR_QUANT_FP8 | AR_QUANT_NVFP4)) && !a.amax_out)
         return;
     float nq[8];

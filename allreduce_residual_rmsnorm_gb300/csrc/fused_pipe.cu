@@ -336,15 +336,15 @@ cudaError_t launch_t(const FusedArgs& a, const LaunchCfg& c)
 
 }  // namespace
 
+// bf16 / fp16 only: fp32 rows take the register-resident row kernels
 bool fused_pipe_supported(int dtype, int H, int R)
 {
-    (void)dtype;
-    return H % 8 == 0 && H <= AR_MAX_HIDDEN && R >= 1 && R <= AR_MAX_RANKS;
+    return (dtype == AR_DT_BF16 || dtype == AR_DT_FP16) && H % 8 == 0 && H <= AR_MAX_HIDDEN && R >= 1 && R <= AR_MAX_RANKS;
 }
 
 cudaError_t launch_fused_pipe(int dtype, const FusedArgs& a, const LaunchCfg& c)
 {
-    if (a.lamport || a.amax_out)
+    if (a.lamport || a.amax_out || !fused_pipe_supported(dtype, a.H, a.R))
         return cudaErrorNotSupported;
     return dtype == AR_DT_BF16 ? launch_t<Bf16>(a, c) : launch_t<Fp16>(a, c);
 }

@@ -8,9 +8,10 @@
 //   rstd = 1 / sqrt(ss / H + eps)           (IEEE div / sqrt)
 //   n = rnd((y * rstd) * gamma)             -> norm_out, FP8 / NVFP4 codes
 //
-// Each row is split into 16-byte vectors of 8 elements; the thread with index
-// g in its group of G threads owns vectors v = g + k*G (k < VPT), so every
-// warp-wide load or store instruction covers 512 contiguous bytes.  The
+// Each row is split into vectors of 8 elements (16 bytes, or 32 bytes of
+// fp32 moved by 256-bit accesses); the thread with index g in its group of G
+// threads owns vectors v = g + k*G (k < VPT), so every warp-wide load or store
+// instruction covers 512 (1024) contiguous bytes.  The
 // summed row stays in registers between the sum of squares and the
 // normalisation: every input byte is read once.  An NVFP4 block (16
 // elements) is the vector pair (2j, 2j+1), held by neighbouring lanes, so the
@@ -27,19 +28,28 @@
 
 namespace arf {
 
-// Block size bound: one vector per thread rows use up to 896 threads (72
-// registers each) with up to 8 ranks, 1024 threads (64 registers) with up to
-// 4; wider rows (several vectors per thread) at most 512.
-template <int RMAX, int VPT, bool WARP_ROW>
+// Threads of a one-vector-per-thread row block: bf16 / fp16 up to 896 (72
+// registers each) with up to 8 ranks, 1024 (64 registers) with up to 4; fp32
+// vectors take twice the registers: up to 512.
+template <class D>
+__host__ __device__ constexpr int one_vec_threads(int rmax)
+{
+    return D::bytes == 4 ? 512 : (rmax <= 4 ? 1024 : 896);
+}
+
+// Block size bound: one_vec_threads for one vector per thread; wider rows
+// (several vectors per thread) at most 512; one row per warp: 8 warps.
+template <class D, int RMAX, int VPT, bool WARP_ROW>
 constexpr int rows_max_threads()
 {
-    return WARP_ROW ? 256 : (VPT == 1 ? (RMAX <= 4 ? 1024 : 896) : 512);
+    return WARP_ROW ? 256 : (VPT == 1 ? one_vec_threads<D>(RMAX) : 512);
 }
 
 // s[kk] (+)= rank batch r0..r0+RB-1 of vector g + (k0 + kk) * G; ELEM rounds
 // every partial sum to the element type.
 template <class D, int KCH, int RB, bool ELEM>
-__device__ __forceinline__ void fold_ranks(float (&s)[KCH][8], const uint4 (&raw)[KCH][RB], int r0,
+__device__ __forceinline__ void fold_ranks(float (&s)[KCH][8],
+                                           const typename D::Vec (&raw)[KCH][RB], int r0,
                                            int R, int g, int k0, int G, int Hv)
 {
 #pragma unroll
@@ -65,13 +75,21 @@ __device__ __forceinline__ void fold_ranks(float (&s)[KCH][8], const uint4 (&raw
 // spans its CTAs (a separate instantiation, so the common one-CTA-per-row
 // kernel carries none of the cluster code).
 template <class D, int RMAX, int VPT, bool WARP_ROW, bool CLUSTER = false>
-__global__ void __launch_bounds__(rows_max_threads<RMAX, VPT, WARP_ROW>())
+__global__ void __launch_bounds__(rows_max_threads<D, RMAX, VPT, WARP_ROW>())
 fused_rows_kernel(const FusedArgs a)
 {
-    // ranks loaded per batch (at most 8 x 16 B of partials in flight per vector)
-    constexpr int RB = RMAX < 8 ? RMAX : 8;
-    // vectors per batch: about 16 partial loads in flight per thread
-    constexpr int KCH = (16 / RB) > VPT ? VPT : (16 / RB);
+    using V = typename D::Vec;
+    constexpr int EB = D::bytes;           // element bytes
+    constexpr int VB = 8 * EB;             // vector bytes
+    // partial vectors in flight per thread: 16 x 16 B (bf16 / fp16); fp32
+    // 4 x 32 B, which keeps its wider vectors within 128 registers (512
+    // threads x 128 B is still ~64 KB in flight per SM)
+    constexpr int LOADS = EB == 4 ? 4 : 16;
+    // ranks loaded per batch
+    constexpr int RBMAX = EB == 4 ? 4 : 8;
+    constexpr int RB = RMAX < RBMAX ? RMAX : RBMAX;
+    // vectors per batch
+    constexpr int KCH = (LOADS / RB) > VPT ? VPT : (LOADS / RB);
     static_assert(VPT % KCH == 0, "batch must divide VPT");
     static_assert(RMAX % RB == 0, "rank batch must divide RMAX");
 
@@ -110,14 +128,14 @@ fused_rows_kernel(const FusedArgs a)
     // register copy) or, in Lamport mode, slot + r * plane
     uint32_t flag = 0;
     const uint8_t* slot = nullptr;
-    const size_t plane = (size_t)a.T * H * 2;
+    const size_t plane = (size_t)a.T * H * EB;
     if (a.lamport) {
         flag = *reinterpret_cast<volatile uint32_t*>(&a.state->lamport_flag);
         const uint64_t clear_elems = *reinterpret_cast<volatile uint64_t*>(&a.state->clear_size);
         slot = a.lamport_base + (size_t)(flag % 3u) * a.slot_bytes;
         // refill the retired slot with the sentinel (clear loop of the one-shot kernel)
         uint8_t* clr = a.lamport_base + (size_t)((flag + 2u) % 3u) * a.slot_bytes;
-        const uint64_t nvec = clear_elems / 8;
+        const uint64_t nvec = clear_elems * EB / 16;
         const uint64_t nth = (uint64_t)gridDim.x * blockDim.x;
         const uint4 sent = make_uint4(0x80000000u, 0x80000000u, 0x80000000u, 0x80000000u);
         for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += nth)
@@ -136,9 +154,9 @@ fused_rows_kernel(const FusedArgs a)
     float amax_local = 0.0f;
 
     for (; row < a.T; row += row_step) {
-        const size_t roff = (size_t)row * H * 2;
+        const size_t roff = (size_t)row * H * EB;
         DF ss = {0.0f, 0.0f};
-        uint4 yv[VPT];
+        V yv[VPT];
 
         // One-row-per-block, staged or caller partials: while this row is
         // loaded and reduced, have the copy engine pull the block's next row
@@ -149,24 +167,25 @@ fused_rows_kernel(const FusedArgs a)
         if (!WARP_ROW && !a.lamport && threadIdx.x < (unsigned)(R + 1)) {
             const int nrow = row + row_step;
             // this CTA's slice of the row (the whole row without a cluster)
-            const size_t off = (size_t)(g - threadIdx.x) * VPT * 16;
-            const size_t len = (size_t)blockDim.x * VPT * 16;
-            if (nrow < a.T && off < (size_t)H * 2) {
+            const size_t off = (size_t)(g - threadIdx.x) * VPT * VB;
+            const size_t len = (size_t)blockDim.x * VPT * VB;
+            const size_t rowb = (size_t)H * EB;
+            if (nrow < a.T && off < rowb) {
                 const uint8_t* src = (int)threadIdx.x < R ? AR_RANK_PTR(threadIdx.x) : a.residual_in;
-                const size_t n = off + len <= (size_t)H * 2 ? len : (size_t)H * 2 - off;
-                prefetch_l2_bulk(src + (size_t)nrow * H * 2 + off, (uint32_t)n);
+                const size_t n = off + len <= rowb ? len : rowb - off;
+                prefetch_l2_bulk(src + (size_t)nrow * rowb + off, (uint32_t)n);
             }
         }
 
 #pragma unroll
         for (int k0 = 0; k0 < VPT; k0 += KCH) {
             float s[KCH][8];
-            uint4 xr[KCH];
+            V xr[KCH];
 #pragma unroll
             for (int r0 = 0; r0 < RMAX; r0 += RB) {
                 if (r0 >= R)
                     break;
-                uint4 raw[KCH][RB];
+                V raw[KCH][RB];
                 // ---- loads of this batch (all in flight together)
 #pragma unroll
                 for (int kk = 0; kk < KCH; ++kk) {
@@ -175,10 +194,10 @@ fused_rows_kernel(const FusedArgs a)
 #pragma unroll
                         for (int rr = 0; rr < RB; ++rr)
                             if (r0 + rr < R)
-                                raw[kk][rr] = a.lamport ? ld_poll(AR_RANK_PTR(r0 + rr) + roff + (size_t)v * 16)
-                                                        : ld_stream(AR_RANK_PTR(r0 + rr) + roff + (size_t)v * 16);
+                                raw[kk][rr] = a.lamport ? ld_poll_v<D>(AR_RANK_PTR(r0 + rr) + roff + (size_t)v * VB)
+                                                        : ld_stream_v<D>(AR_RANK_PTR(r0 + rr) + roff + (size_t)v * VB);
                         if (r0 == 0)
-                            xr[kk] = ld_stream(a.residual_in + roff + (size_t)v * 16);
+                            xr[kk] = ld_stream_v<D>(a.residual_in + roff + (size_t)v * VB);
                     }
                 }
                 // ---- Lamport: re-poll until no sentinel word is left (bounded)
@@ -201,7 +220,7 @@ fused_rows_kernel(const FusedArgs a)
 #pragma unroll
                                 for (int rr = 0; rr < RB; ++rr)
                                     if (r0 + rr < R && v < Hv && has_sentinel(raw[kk][rr])) {
-                                        raw[kk][rr] = ld_poll(AR_RANK_PTR(r0 + rr) + roff + (size_t)v * 16);
+                                        raw[kk][rr] = ld_poll_v<D>(AR_RANK_PTR(r0 + rr) + roff + (size_t)v * VB);
                                         if (has_sentinel(raw[kk][rr])) {
                                             pend = true;
                                             if (first < 0)
@@ -232,12 +251,12 @@ fused_rows_kernel(const FusedArgs a)
                 const int k = k0 + kk;
                 const int v = g + k * G;
                 if (v < Hv) {
-                    const uint4 y = residual_vec<D>(s[kk], xr[kk], ss);
+                    const V y = residual_vec<D>(s[kk], xr[kk], ss);
                     yv[k] = y;
                     if (pat & AR_RESIDUAL_OUT)
-                        st_vec(a.residual_out + roff + (size_t)v * 16, y);
+                        st_vec(a.residual_out + roff + (size_t)v * VB, y);
                 } else {
-                    yv[k] = make_uint4(0, 0, 0, 0);
+                    yv[k] = zero_vec<V>();
                 }
             }
         }

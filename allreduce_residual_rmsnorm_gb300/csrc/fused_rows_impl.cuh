@@ -105,10 +105,11 @@ static inline int pow2_at_least(int x)
 // Geometry:
 //   WARP_ROW: 8 warps per block, one row per warp, VPT = ceil(Hv / 32) in
 //             {1, 2, 4} (hidden <= 1024).
-//   CTA_ROW : one row per block; one vector per thread up to 896 threads
-//             (hidden <= 7168; up to 1024 threads, hidden <= 8192, with at
-//             most 4 ranks), else VPT in {2, 4, 8} with <= 512 threads
-//             (hidden <= 32768).
+//   CTA_ROW : one row per block; one vector per thread up to
+//             one_vec_threads (bf16 / fp16: 896 threads, hidden <= 7168, or
+//             1024 threads, hidden <= 8192, with at most 4 ranks; fp32: 512
+//             threads, hidden <= 4096), else VPT in {2, 4, 8} with <= 512
+//             threads (hidden <= 32768).
 //             With LaunchCfg::cluster = C > 1, one row per cluster of C CTAs
 //             (one vector per thread, the row's sum of squares combined through
 //             distributed shared memory) for token counts below the SM count.
@@ -134,7 +135,7 @@ cudaError_t launch_fused_rows_t(int variant, const FusedArgs& a, const LaunchCfg
     } else {
         // one vector per thread up to 896 threads, else <= 512 threads
         // (two vectors per thread measured 208 us vs 188 us at H = 7168)
-        const int one_vec_max = rmax <= 4 ? 1024 : 896;
+        const int one_vec_max = one_vec_threads<D>(rmax);
         // a row split over a cluster of C CTAs: one vector per thread only
         if (C > 1 && (Hv + C - 1) / C > one_vec_max)
             C = 1;

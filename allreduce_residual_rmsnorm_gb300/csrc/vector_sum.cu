@@ -2,10 +2,11 @@
 // (mscclpp allreduce.cu: vectorSum, here out of place over R inputs and with
 // fp32 accumulation).
 //
-// 16-byte aligned inputs: grid-stride over 16-byte vectors, two vectors per
-// thread per step so 2R loads are in flight, and the n % 8 tail elements done
-// one by one (the page's vectorSum drops nothing either: its 32-bit tail loop
-// covers the rest).  Any misaligned pointer: element-wise kernel.
+// Vector-aligned inputs (16 bytes; 32 for fp32): grid-stride over vectors of
+// 8 elements, two vectors per thread per step so 2R loads are in flight, and
+// the n % 8 tail elements done one by one (the page's vectorSum drops nothing
+// either: its 32-bit tail loop covers the rest).  Any misaligned pointer:
+// element-wise kernel.
 #include "ar_common.cuh"
 #include "ar_internal.h"
 
@@ -14,6 +15,8 @@ namespace arf {
 template <class D>
 __device__ __forceinline__ float ld_elem(const uint8_t* p, uint64_t i)
 {
+    if constexpr (D::bytes == 4)
+        return reinterpret_cast<const float*>(p)[i];
     const uint16_t b = reinterpret_cast<const uint16_t*>(p)[i];
     if constexpr (D::id == AR_DT_BF16) {
         return __uint_as_float((uint32_t)b << 16);
@@ -27,6 +30,10 @@ __device__ __forceinline__ float ld_elem(const uint8_t* p, uint64_t i)
 template <class D>
 __device__ __forceinline__ void st_elem(uint8_t* p, uint64_t i, float v)
 {
+    if constexpr (D::bytes == 4) {
+        reinterpret_cast<float*>(p)[i] = v;
+        return;
+    }
     uint16_t b;
     if constexpr (D::id == AR_DT_BF16) {
         __nv_bfloat16 h = __float2bfloat16_rn(v);
@@ -42,14 +49,17 @@ __device__ __forceinline__ void st_elem(uint8_t* p, uint64_t i, float v)
 template <class D>
 __device__ __forceinline__ float round1(float v)
 {
-    if constexpr (D::id == AR_DT_BF16)
+    if constexpr (D::bytes == 4)
+        return v;
+    else if constexpr (D::id == AR_DT_BF16)
         return __bfloat162float(__float2bfloat16_rn(v));
     else
         return __half2float(__float2half_rn(v));
 }
 
 template <class D, int RMAX>
-__device__ __forceinline__ uint4 sum_vec(const SumArgs& a, const uint4 (&raw)[RMAX])
+__device__ __forceinline__ typename D::Vec sum_vec(const SumArgs& a,
+                                                   const typename D::Vec (&raw)[RMAX])
 {
     float s[8];
     unpack8<D>(raw[0], s);
@@ -71,29 +81,31 @@ __device__ __forceinline__ uint4 sum_vec(const SumArgs& a, const uint4 (&raw)[RM
 template <class D, int RMAX>
 __global__ void __launch_bounds__(256) vector_sum_kernel(const SumArgs a)
 {
+    using V = typename D::Vec;
+    constexpr uint64_t VB = 8 * D::bytes;
     const uint64_t nvec = a.n / 8;
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
     const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
     uint64_t i = tid;
     for (; i + stride < nvec; i += 2 * stride) {
-        uint4 r0[RMAX], r1[RMAX];
+        V r0[RMAX], r1[RMAX];
 #pragma unroll
         for (int r = 0; r < RMAX; ++r) {
             if (r < a.R) {
-                r0[r] = ld_stream(a.in[r] + i * 16);
-                r1[r] = ld_stream(a.in[r] + (i + stride) * 16);
+                r0[r] = ld_stream_v<D>(a.in[r] + i * VB);
+                r1[r] = ld_stream_v<D>(a.in[r] + (i + stride) * VB);
             }
         }
-        st_vec(a.out + i * 16, sum_vec<D, RMAX>(a, r0));
-        st_vec(a.out + (i + stride) * 16, sum_vec<D, RMAX>(a, r1));
+        st_vec(a.out + i * VB, sum_vec<D, RMAX>(a, r0));
+        st_vec(a.out + (i + stride) * VB, sum_vec<D, RMAX>(a, r1));
     }
     if (i < nvec) {
-        uint4 r0[RMAX];
+        V r0[RMAX];
 #pragma unroll
         for (int r = 0; r < RMAX; ++r)
             if (r < a.R)
-                r0[r] = ld_stream(a.in[r] + i * 16);
-        st_vec(a.out + i * 16, sum_vec<D, RMAX>(a, r0));
+                r0[r] = ld_stream_v<D>(a.in[r] + i * VB);
+        st_vec(a.out + i * VB, sum_vec<D, RMAX>(a, r0));
     }
     const uint64_t tail = a.n - nvec * 8;
     if (tid < tail) {
@@ -138,9 +150,10 @@ static const void* sum_fn(int rmax)
 template <class D>
 static cudaError_t launch_t(const SumArgs& a, const LaunchCfg& c)
 {
-    bool aligned = ((uintptr_t)a.out & 15) == 0;
+    constexpr uintptr_t vmask = 8 * D::bytes - 1;
+    bool aligned = ((uintptr_t)a.out & vmask) == 0;
     for (int r = 0; r < a.R; ++r)
-        aligned = aligned && ((uintptr_t)a.in[r] & 15) == 0;
+        aligned = aligned && ((uintptr_t)a.in[r] & vmask) == 0;
     const int threads = 256;
     void* args[] = {const_cast<SumArgs*>(&a)};
     if (!aligned) {
@@ -155,7 +168,7 @@ static cudaError_t launch_t(const SumArgs& a, const LaunchCfg& c)
     }
     const int rmax = a.R <= 2 ? 2 : a.R <= 4 ? 4 : a.R <= 8 ? 8 : 16;
     const void* fn = sum_fn<D>(rmax);
-    static int cached[2][17] = {};                 // blocks per SM, per type and RMAX
+    static int cached[3][17] = {};                 // blocks per SM, per type and RMAX
     int per_sm = cached[D::id][rmax];
     if (per_sm == 0) {
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, 0) != cudaSuccess ||
@@ -176,7 +189,12 @@ static cudaError_t launch_t(const SumArgs& a, const LaunchCfg& c)
 
 cudaError_t launch_vector_sum(int dtype, const SumArgs& a, const LaunchCfg& c)
 {
-    return dtype == AR_DT_BF16 ? launch_t<Bf16>(a, c) : launch_t<Fp16>(a, c);
+    switch (dtype) {
+    case AR_DT_BF16: return launch_t<Bf16>(a, c);
+    case AR_DT_FP16: return launch_t<Fp16>(a, c);
+    case AR_DT_FP32: return launch_t<F32>(a, c);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace arf

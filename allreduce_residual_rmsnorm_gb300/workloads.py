@@ -10,7 +10,7 @@ Recipe (one CPU ``torch.Generator`` seeded with ``seed``, draws in this order):
       if heavy_frac > 0:
           u_r  = rand(T, H);  hv_r = randn(T, H) * heavy_std
           base_r[u_r < heavy_frac] = hv_r[u_r < heavy_frac]
-      partial_r = base_r rounded (RNE) to D
+      partial_r = base_r rounded (RNE) to D (exact for D = fp32)
   residual = randn(T, H) * x_std  -> D
   gamma    = 1 + randn(H) * g_std  -> D
 Plain R-way sum inputs: for each rank, (rand(N) * 2 - 1) -> D, i.e. U(-1, 1).
@@ -75,9 +75,16 @@ SUMS = [SumWorkload(f"sum_r8_n{n}", R=8, N=n) for n in SUM_SIZES]
 
 FUSED = [TINY, DECODE, FP8_PREFILL, NVFP4_PREFILL]
 
+# fp32 elements (the 4-byte exchange type of fp32 Lamport workspaces): the
+# decode shape above and a prefill-sized row set with NVFP4 output.
+FP32_DECODE = FusedWorkload("r8_t128_h4096_fp32_res_norm", R=8, T=128, H=4096, dtype="fp32",
+                            p_std=0.5, eps=1e-5, pattern=RES_NORM)
+FP32_PREFILL = FusedWorkload("r8_t1024_h7168_fp32_res_norm_nvfp4", R=8, T=1024, H=7168,
+                             dtype="fp32", heavy_frac=0.01, eps=1e-6, pattern=RES_NORM_NVFP4)
+
 
 def torch_dtype(name: str) -> torch.dtype:
-    return {"bf16": torch.bfloat16, "fp16": torch.float16}[name]
+    return {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}[name]
 
 
 @dataclass
@@ -122,14 +129,19 @@ def make_sum_inputs(w: SumWorkload) -> torch.Tensor:
 
 
 def bits(t: torch.Tensor):
-    """CPU tensor of a 16-bit float type -> numpy uint16 bit patterns (no copy
-    of values through any float conversion)."""
+    """CPU float tensor -> numpy bit patterns (uint16 for 16-bit types, uint32
+    for fp32; no copy of values through any float conversion)."""
     import numpy as np
+    if t.element_size() == 4:
+        return t.contiguous().view(torch.int32).numpy().view(np.uint32)
     assert t.element_size() == 2
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
 def from_bits(a, dtype: str) -> torch.Tensor:
     import numpy as np
+    if dtype == "fp32":
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint32).view(np.int32)).view(
+            torch.float32)
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint16).view(np.int16)).view(
         torch_dtype(dtype))

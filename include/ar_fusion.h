@@ -3,7 +3,7 @@
  * (libarfusion.so, sm_103a).
  *
  * The operation (per token row t of a [tokens][hidden] problem, element type D
- * = bf16 or fp16):
+ * = bf16, fp16 or fp32; round_D is the identity for fp32):
  *
  *   s_h  = P_0[t][h] + P_1[t][h] + ... + P_{R-1}[t][h]  (fp32, rank order)
  *   a_h  = round_D(s_h)
@@ -39,7 +39,8 @@
  *   - Every call returns an ar_status code and never throws or aborts.  Invalid
  *     arguments are rejected before anything is launched.  The message for the
  *     last failure on the calling thread is ar_fusion_last_error().
- *   - All device pointers must be 16-byte aligned (AR_ERR_INVALID otherwise).
+ *   - All device pointers must be 16-byte aligned, fp32 element arrays 32-byte
+ *     aligned (AR_ERR_INVALID otherwise).
  *   - The caller owns every tensor; the library owns the workspace object and,
  *     unless the caller supplied it, the workspace memory.
  *   - Device-side waits are bounded: a wait that gives up records
@@ -58,10 +59,17 @@ extern "C" {
 
 /* ------------------------------------------------------------ constants -- */
 
-/* Element types of partials, residual, gamma and the 16-bit outputs. */
+/* Element types of partials, residual, gamma and the residual / norm
+ * outputs.  AR_DT_FP32 is the 4-byte exchange type of FlashInfer's
+ * trtllm_create_ipc_workspace_for_all_reduce_fusion(use_fp32_lamport=True):
+ * the workspace regions hold fp32 elements, and every rounding to the element
+ * type is the identity.  fp32 device pointers (partials, residual_in, gamma,
+ * residual_out, norm_out; fp32 sum inputs and output on the vector path) must
+ * be 32-byte aligned. */
 enum ar_dtype {
     AR_DT_BF16 = 0,
-    AR_DT_FP16 = 1
+    AR_DT_FP16 = 1,
+    AR_DT_FP32 = 2
 };
 
 /* Output pattern bits.  Valid patterns are the four of allreduce_fusion_op
@@ -138,7 +146,7 @@ typedef struct ar_fusion_ws_info {
     int32_t max_token_num;
     int32_t hidden_dim;
     int32_t dtype;                 /* enum ar_dtype */
-    int32_t elem_bytes;            /* 2 */
+    int32_t elem_bytes;            /* sizeof(D): 2, or 4 for AR_DT_FP32 */
     int32_t oneshot_max_tokens;    /* AR_ONESHOT_MAX_TOKENS */
     uint64_t total_bytes;          /* whole workspace */
     uint64_t buffer_bytes;         /* R * max_token_num * hidden * elem */
@@ -324,8 +332,8 @@ int ar_fusion_norm_amax(ar_fusion_ws* ws, const void* const* partials, int nrank
  *   bufs    host array of `nranks` device pointers, n elements of D each
  *   nranks  1..AR_MAX_RANKS;  n any size (no alignment tail restriction)
  *   out     n elements of D; may alias none of the inputs
- * Pointers need only element alignment here; 16-byte aligned inputs take the
- * 128-bit path.  Errors: AR_ERR_INVALID, AR_ERR_UNSUPPORTED, AR_ERR_CUDA. */
+ * Pointers need only element alignment here; 16-byte aligned inputs (bf16,
+ * fp16) or 32-byte aligned inputs (fp32) take the vector path.  Errors: AR_ERR_INVALID, AR_ERR_UNSUPPORTED, AR_ERR_CUDA. */
 int ar_fusion_sum(const void* const* bufs, int nranks, size_t n, int dtype, void* out,
                   void* stream);
 
@@ -359,7 +367,7 @@ int ar_fusion_sum_ex(const void* const* bufs, int nranks, size_t n, int dtype, i
  * slot index -- all on `stream`.  Nothing is allocated: no cudaMalloc,
  * cudaFree or allocating library call.
  *
- * Limits: nranks * tokens * hidden_dim * 2 <= AR_NOALLOC_SLOT_BYTES, else
+ * Limits: nranks * tokens * hidden_dim * sizeof(D) <= AR_NOALLOC_SLOT_BYTES, else
  * AR_ERR_CAPACITY before anything runs.  Other argument rules and errors as
  * ar_fusion_run.
  * Set-up: the first call on each device (the device current at the call)

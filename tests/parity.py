@@ -1,9 +1,9 @@
 """Helpers shared by the GPU parity tests: run a workload through the C ABI
 and through the CPU oracle, and compare under the stated tolerances.
 
-Tolerances (per element, bf16 / fp16): |g - o| <= atol + rtol * |o| with
-(2e-2, 1e-2) for bf16 and (5e-3, 5e-3) for fp16.  Quantised codes must be
-bit-exact except that at most 0.1% may differ by one code step.
+Tolerances (per element): |g - o| <= atol + rtol * |o| with (2e-2, 1e-2) for
+bf16, (5e-3, 5e-3) for fp16 and (1e-5, 1e-5) for fp32.  Quantised codes must
+be bit-exact except that at most 0.1% may differ by one code step.
 """
 from __future__ import annotations
 
@@ -14,19 +14,41 @@ import oracle
 from allreduce_residual_rmsnorm_gb300 import binding as B
 from allreduce_residual_rmsnorm_gb300 import workloads as W
 
-TOL = {"bf16": (2e-2, 1e-2), "fp16": (5e-3, 5e-3)}
+TOL = {"bf16": (2e-2, 1e-2), "fp16": (5e-3, 5e-3), "fp32": (1e-5, 1e-5)}
 ODT = {"bf16": oracle.BF16, "fp16": oracle.FP16}
-BDT = {"bf16": B.AR_DT_BF16, "fp16": B.AR_DT_FP16}
+BDT = {"bf16": B.AR_DT_BF16, "fp16": B.AR_DT_FP16, "fp32": B.AR_DT_FP32}
 
 
 def to_float(bits16: np.ndarray, dtype: str) -> np.ndarray:
     return W.from_bits(bits16, dtype).float().numpy()
 
 
+def oracle_expected_f32(w: W.FusedWorkload, inp: W.FusedInputs, lamport_flip: bool = False):
+    """oracle_expected for fp32 elements (residual / norm as uint32 bits)."""
+    P = inp.partials.numpy()
+    if lamport_flip:
+        P = oracle.lamport_flip(P.view(np.uint16)).view(np.float32)
+    res, nrm, rstd = oracle.fused_f32(P, inp.residual.numpy(), inp.gamma.numpy(), inp.eps)
+    out = {"residual": res.view(np.uint32), "norm": nrm.view(np.uint32), "rstd": rstd}
+    pat = B.PATTERNS[w.pattern]
+    if pat & (B.AR_QUANT_FP8 | B.AR_QUANT_NVFP4):
+        amax = oracle.amax_f32(nrm)
+        out["amax"] = amax
+        if pat & B.AR_QUANT_FP8:
+            out["scale"] = oracle.fp8_inv_scale(amax)
+            out["quant"] = oracle.quant_fp8_f32(nrm, out["scale"])
+        else:
+            out["scale"] = oracle.nvfp4_global_scale(amax)
+            out["quant"], out["sf"] = oracle.quant_nvfp4_f32(nrm, out["scale"])
+    return out
+
+
 def oracle_expected(w: W.FusedWorkload, inp: W.FusedInputs, lamport_flip: bool = False,
                     acc: int = 0):
     """Oracle outputs for the workload: dict with residual, norm, amax and,
     when quantised, the scale passed to both sides and the codes."""
+    if w.dtype == "fp32":
+        return oracle_expected_f32(w, inp, lamport_flip)
     odt = ODT[w.dtype]
     P = W.bits(inp.partials)
     if lamport_flip:

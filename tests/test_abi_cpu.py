@@ -66,6 +66,9 @@ def test_workspace_bytes_validation(L):
         assert rc == code, (args, _err(rc))
         assert B.ar_fusion_last_error()
     assert L.ar_fusion_workspace_bytes(2, 16, 512, 0, None) == B.AR_ERR_INVALID
+    # fp32 elements: the same regions with 4-byte elements
+    assert L.ar_fusion_workspace_bytes(8, 8192, 7168, B.AR_DT_FP32, ctypes.byref(n)) == B.AR_OK
+    assert n.value == up(up(up(2 * buf) + flags) + 3 * 2 * slot + 56)
 
 
 def test_create_rejects_bad_shapes_before_cuda(L):
@@ -103,6 +106,10 @@ def test_sum_validation(L):
     assert L.ar_fusion_sum(arr, 2, 10, 3, ctypes.c_void_p(64), None) == B.AR_ERR_UNSUPPORTED
     assert L.ar_fusion_sum(arr, 2, 0, 0, ctypes.c_void_p(64), None) == B.AR_OK     # empty: no launch
     assert L.ar_fusion_sum_ex(arr, 2, 10, 0, 7, ctypes.c_void_p(64), None) == B.AR_ERR_INVALID
+    # fp32 needs 4-byte element alignment
+    assert L.ar_fusion_sum(arr, 2, 10, B.AR_DT_FP32, ctypes.c_void_p(66), None) == B.AR_ERR_INVALID
+    odd = (ctypes.c_void_p * 2)(16, 34)
+    assert L.ar_fusion_sum(odd, 2, 10, B.AR_DT_FP32, ctypes.c_void_p(64), None) == B.AR_ERR_INVALID
     assert L.ar_fusion_sum(arr, 2, 10, 0, None, None) == B.AR_ERR_INVALID
     bad = (ctypes.c_void_p * 2)(16, 33)
     assert L.ar_fusion_sum(bad, 2, 10, 0, ctypes.c_void_p(64), None) == B.AR_ERR_INVALID

@@ -30,8 +30,9 @@ from allreduce_residual_rmsnorm_gb300 import workloads as W
 def _outputs(w, dev="cuda"):
     T, H = w.T, w.H
     pat = B.PATTERNS[w.pattern]
-    out = {"residual": torch.full((T, H), float("nan"), dtype=torch.bfloat16, device=dev),
-           "norm": torch.full((T, H), float("nan"), dtype=torch.bfloat16, device=dev),
+    dt = W.torch_dtype(w.dtype)
+    out = {"residual": torch.full((T, H), float("nan"), dtype=dt, device=dev),
+           "norm": torch.full((T, H), float("nan"), dtype=dt, device=dev),
            "quant": None, "sf": None}
     if pat & B.AR_QUANT_FP8:
         out["quant"] = torch.full((T, H), 0xAA, dtype=torch.uint8, device=dev)
@@ -52,6 +53,8 @@ CASES = [
     W.TINY,                                                             # 2 x 16 x 512
     W.FusedWorkload("noalloc_nvfp4", R=8, T=32, H=2048, pattern=W.RES_NORM_NVFP4, heavy_frac=0.01),
     W.FusedWorkload("noalloc_fp8", R=4, T=24, H=4096, pattern=W.RES_QUANT_FP8),
+    W.FusedWorkload("noalloc_fp32_nvfp4", R=4, T=16, H=4096, dtype="fp32",
+                    pattern=W.RES_NORM_NVFP4),                           # 1 MiB per slot
 ]
 
 
@@ -61,7 +64,8 @@ def test_noalloc_matches_workspace_call_twice(w):
     B.load()
     L = B.lib()
     pat = B.PATTERNS[w.pattern]
-    ws = B.ar_fusion_workspace_create(w.R, w.T, w.H, B.AR_DT_BF16)
+    dtype = PY.BDT[w.dtype]
+    ws = B.ar_fusion_workspace_create(w.R, w.T, w.H, dtype)
     stream = torch.cuda.current_stream().cuda_stream
     for call in range(2):
         inp = W.make_fused_inputs(w.with_(seed=1000 + call))
@@ -78,7 +82,7 @@ def test_noalloc_matches_workspace_call_twice(w):
         def ptr(t):
             return None if t is None else t.data_ptr()
 
-        rc = L.ar_fusion_run_noalloc(parts, w.R, w.T, w.H, B.AR_DT_BF16, X.data_ptr(),
+        rc = L.ar_fusion_run_noalloc(parts, w.R, w.T, w.H, dtype, X.data_ptr(),
                                      G.data_ptr(), ctypes.c_float(w.eps), pat,
                                      ptr(got["residual"]), ptr(got["norm"]), ptr(got["quant"]),
                                      ptr(got["sf"]), scale.data_ptr(), stream)
@@ -86,9 +90,10 @@ def test_noalloc_matches_workspace_call_twice(w):
         torch.cuda.synchronize()
         exp_h, got_h = _host(ref, pat), _host(got, pat)
         if pat & B.AR_RESIDUAL_OUT:
-            PY.assert_close16(got_h["residual"], exp_h["residual"], "bf16", f"residual (call {call})")
+            PY.assert_close16(got_h["residual"], exp_h["residual"], w.dtype,
+                              f"residual (call {call})")
         if pat & B.AR_NORM_OUT:
-            PY.assert_close16(got_h["norm"], exp_h["norm"], "bf16", f"norm (call {call})")
+            PY.assert_close16(got_h["norm"], exp_h["norm"], w.dtype, f"norm (call {call})")
         if pat & B.AR_QUANT_FP8:
             PY.assert_codes(got_h["quant"], exp_h["quant"], "e4m3", f"fp8 (call {call})")
         if pat & B.AR_QUANT_NVFP4:
@@ -109,4 +114,8 @@ def test_noalloc_rejects_sizes_beyond_the_scratch_before_any_cuda_call():
     rc = L.ar_fusion_run_noalloc(big, 17, 1, 64, B.AR_DT_BF16, 16, 16, ctypes.c_float(1e-5),
                                  B.PATTERNS["res_norm"], 16, 16, None, None, None, None)
     assert rc == B.AR_ERR_UNSUPPORTED
+    # fp32 elements count 4 bytes: 8 x 64 x 4096 x 4 = 8 MiB
+    rc = L.ar_fusion_run_noalloc(big, 8, 64, 4096, B.AR_DT_FP32, 32, 32, ctypes.c_float(1e-5),
+                                 B.PATTERNS["res_norm"], 32, 32, None, None, None, None)
+    assert rc == B.AR_ERR_CAPACITY
     assert np.int64(B.AR_NOALLOC_SLOT_BYTES) == 4 << 20
