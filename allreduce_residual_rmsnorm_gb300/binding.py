@@ -80,7 +80,7 @@ class WsInfo(ctypes.Structure):
         ("lamport_buffer_bytes", ctypes.c_uint64), ("state_bytes", ctypes.c_uint64),
         ("base", ctypes.c_void_p), ("buffer", ctypes.c_void_p), ("flags", ctypes.c_void_p),
         ("lamport", ctypes.c_void_p), ("state", ctypes.c_void_p),
-        ("last_variant", ctypes.c_int32), ("pad0", ctypes.c_int32),
+        ("last_variant", ctypes.c_int32), ("last_cluster", ctypes.c_int32),
     ]
 
 

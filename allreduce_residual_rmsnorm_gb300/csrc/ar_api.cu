@@ -46,7 +46,7 @@ struct ar_fusion_ws {
     uint8_t* base;
     uint64_t total, buffer_off, buffer_bytes, flag_off, flag_bytes, lamport_off, slot_bytes,
         state_off;
-    int variant, mode, last_variant;
+    int variant, mode, last_variant, last_cluster;
     uint64_t timeout_ns;
     int cluster, pdl;           // launch options of the fused call (0 cluster = auto)
     int acc;                    // AR_ACC_FP32 or AR_ACC_ELEMENT
@@ -337,13 +337,33 @@ int pick_variant(const ar_fusion_ws* ws, const FusedArgs& a)
     return a.H <= 512 ? AR_VARIANT_WARP_ROW : AR_VARIANT_CTA_ROW;
 }
 
+// CTAs per row when the caller left the choice to the library (cluster 0).
+// fp32 rows of more than 512 vectors (hidden > 4096) would need two vectors
+// per thread in one CTA; with more than 4 ranks, splitting each row over a
+// cluster of 2 CTAs (one vector per thread) is faster: at R = 8, H = 7168,
+// 391.0 vs 494.4 us (8192 tokens) and 60.6 vs 70.0 us (1024 tokens).  With 4
+// ranks (H = 8192: 88.1 vs 80.8 us) and for every bf16 / fp16 case measured
+// (e.g. R = 8, T = 8192, H = 7168: 231.8 vs 180.1 us) one CTA per row wins.
+int auto_cluster(const ar_fusion_ws* ws, const FusedArgs& a, int variant)
+{
+    if (ws->cluster > 0)
+        return ws->cluster;
+    const int Hv = a.H / 8;
+    if (ws->dtype == AR_DT_FP32 && variant == AR_VARIANT_CTA_ROW && a.R > 4 && Hv > 512 &&
+        Hv <= 1024 && a.T >= 256)
+        return 2;
+    return 1;
+}
+
 int launch_fused(ar_fusion_ws* ws, const FusedArgs& a, cudaStream_t s)
 {
     LaunchCfg c{ws->sms, s};
-    c.cluster = ws->cluster > 0 ? ws->cluster : 1;
     c.pdl = ws->pdl;
     const int variant = pick_variant(ws, a);
+    c.cluster = auto_cluster(ws, a, variant);
     ws->last_variant = variant;
+    ws->last_cluster = 1;
+    c.used_cluster = &ws->last_cluster;
     cudaError_t e = variant == AR_VARIANT_BULK_PIPE ? launch_fused_pipe(ws->dtype, a, c)
                                                     : launch_fused_rows(ws->dtype, variant, a, c);
     if (e != cudaSuccess)
@@ -421,6 +441,7 @@ int ar_fusion_workspace_create(int tp_size, int max_token_num, int hidden_dim, i
     ws->state_off = L.state_off;
     ws->variant = AR_VARIANT_AUTO;
     ws->last_variant = AR_VARIANT_AUTO;
+    ws->last_cluster = 0;
     ws->cluster = 0;
     ws->pdl = 0;
     ws->acc = AR_ACC_FP32;
@@ -495,6 +516,7 @@ int ar_fusion_workspace_info(const ar_fusion_ws* ws, ar_fusion_ws_info* info)
     info->lamport = ws->base + ws->lamport_off;
     info->state = ws->base + ws->state_off;
     info->last_variant = ws->last_variant;
+    info->last_cluster = ws->last_cluster;
     return AR_OK;
 }
 

@@ -36,6 +36,7 @@ struct LaunchCfg {
     cudaStream_t stream;
     int cluster = 1;            // CTAs per row (one-row-per-block kernel), 1, 2, 4 or 8
     int pdl = 0;                // programmatic dependent launch
+    int* used_cluster = nullptr;  // out: CTAs per row the row kernel was launched with
 };
 
 // Kernel launchers (return cudaError_t of the launch).  `variant` is a

@@ -81,12 +81,14 @@ fused_rows_kernel(const FusedArgs a)
     using V = typename D::Vec;
     constexpr int EB = D::bytes;           // element bytes
     constexpr int VB = 8 * EB;             // vector bytes
-    // partial vectors in flight per thread: 16 x 16 B (bf16 / fp16); fp32
-    // 4 x 32 B, which keeps its wider vectors within 128 registers (512
-    // threads x 128 B is still ~64 KB in flight per SM)
-    constexpr int LOADS = EB == 4 ? 4 : 16;
+    // partial vectors in flight per thread: 16 x 16 B (bf16 / fp16), 8 x 32 B
+    // (fp32; within 128 registers at 512 threads).  fp32 batchings measured
+    // at (R, T, H) = (8, 4096, 4096) / (4, 2048, 8192) / (8, 128, 4096):
+    // 8 loads of up to 8 ranks 115.3 / 80.8 / 8.3 us, 4 loads of up to 4
+    // ranks 124.9 / 93.1 / 9.0 us, 2 loads at 1024 threads 154.3 / 86.0 / 9.2 us.
+    constexpr int LOADS = EB == 4 ? 8 : 16;
     // ranks loaded per batch
-    constexpr int RBMAX = EB == 4 ? 4 : 8;
+    constexpr int RBMAX = 8;
     constexpr int RB = RMAX < RBMAX ? RMAX : RBMAX;
     // vectors per batch
     constexpr int KCH = (LOADS / RB) > VPT ? VPT : (LOADS / RB);

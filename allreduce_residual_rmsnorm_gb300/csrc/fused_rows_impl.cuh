@@ -160,6 +160,8 @@ cudaError_t launch_fused_rows_t(int variant, const FusedArgs& a, const LaunchCfg
         return cudaErrorInvalidValue;
     if (grid < 1)
         grid = 1;
+    if (c.used_cluster)
+        *c.used_cluster = C;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     int na = 0;

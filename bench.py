@@ -300,20 +300,22 @@ def run_sweep(args):
 
     def report(w, pat, ws, lam, us, cl, pdl):
         rc, _ = B.ar_fusion_workspace_status(ws)
-        outb = (w.T * w.H * 2 if pat & B.AR_NORM_OUT else 0) + \
+        eb = 4 if w.dtype == "fp32" else 2
+        outb = (w.T * w.H * eb if pat & B.AR_NORM_OUT else 0) + \
                (w.T * w.H if pat & B.AR_QUANT_FP8 else 0) + \
                (w.T * w.H // 2 + w.T * w.H // 16 if pat & B.AR_QUANT_NVFP4 else 0)
-        byts = w.R * w.T * w.H * 2 + w.T * w.H * 2 * (2 if pat & B.AR_RESIDUAL_OUT else 1) + outb
-        last = B.ar_fusion_workspace_info(ws)["last_variant"]
-        print(json.dumps({"sweep": w.name, "mode": "lamport" if lam else "buffer",
+        byts = w.R * w.T * w.H * eb + w.T * w.H * eb * (2 if pat & B.AR_RESIDUAL_OUT else 1) + outb
+        info = B.ar_fusion_workspace_info(ws)
+        last = info["last_variant"]
+        print(json.dumps({"sweep": w.name, "dtype": w.dtype, "mode": "lamport" if lam else "buffer",
                           "variant": {1: "warp_row", 2: "cta_row", 3: "bulk_pipe"}.get(last),
-                          "cluster": cl, "pdl": pdl,
+                          "cluster": cl, "cluster_used": info["last_cluster"], "pdl": pdl,
                           "us": us, "tokens_per_s": w.T / (us * 1e-6), "bytes": byts,
                           "gbs": byts / (us * 1e-6) / 1e9, "frac_of_copy_peak": byts / (us * 1e-6) / 1e9 / peak,
                           "l2": "inputs just staged (L2-resident)" if lam or byts < 129e6 else "inputs > L2",
                           "status": rc}), flush=True)
 
-    for w in W.FUSED:
+    for w in W.FUSED + [W.FP32_DECODE, W.FP32_PREFILL]:
         inp = W.make_fused_inputs(w)
         P, X, G = inp.partials.to(dev), inp.residual.to(dev), inp.gamma.to(dev)
         pat = B.PATTERNS[w.pattern]
@@ -324,7 +326,8 @@ def run_sweep(args):
         if pat & B.AR_QUANT_NVFP4:
             q = torch.empty(w.T, w.H // 2, dtype=torch.uint8, device=dev)
             sf = torch.empty(w.T, w.H // 16, dtype=torch.uint8, device=dev)
-        ws = B.ar_fusion_workspace_create(w.R, w.T, w.H, B.AR_DT_BF16)
+        dt = {"bf16": B.AR_DT_BF16, "fp16": B.AR_DT_FP16, "fp32": B.AR_DT_FP32}[w.dtype]
+        ws = B.ar_fusion_workspace_create(w.R, w.T, w.H, dt)
         lam = w.T <= B.AR_ONESHOT_MAX_TOKENS
         if pat & (B.AR_QUANT_FP8 | B.AR_QUANT_NVFP4):
             amax = torch.empty(1, device=dev)
@@ -358,13 +361,14 @@ def run_sweep(args):
         del P, X, G, out, q, sf
         torch.cuda.empty_cache()
 
-    for sw in W.SUMS:
+    for sw in W.SUMS + [W.SumWorkload("sum_r8_n67108864_fp32", R=8, N=64 << 20, dtype="fp32")]:
         x = W.make_sum_inputs(sw).to(dev)
-        out = torch.empty(sw.N, dtype=torch.float16, device=dev)
+        out = torch.empty(sw.N, dtype=x.dtype, device=dev)
         bufs = [x[r] for r in range(sw.R)]
         us = graph_us(lambda: B.ar_fusion_sum(bufs, out))
-        byts = (sw.R + 1) * sw.N * 2
-        print(json.dumps({"sweep": sw.name, "us": us, "bytes": byts, "gbs": byts / (us * 1e-6) / 1e9,
+        byts = (sw.R + 1) * sw.N * x.element_size()
+        print(json.dumps({"sweep": sw.name, "dtype": sw.dtype, "us": us, "bytes": byts,
+                          "gbs": byts / (us * 1e-6) / 1e9,
                           "frac_of_copy_peak": byts / (us * 1e-6) / 1e9 / peak,
                           "l2": "inputs > L2" if byts > 129e6 else "L2-resident (warm)"}), flush=True)
         del x, out

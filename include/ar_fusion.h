@@ -160,7 +160,7 @@ typedef struct ar_fusion_ws_info {
     void* lamport;                 /* slot k at lamport + k * lamport_comm_bytes */
     void* state;                   /* struct ar_fusion_state */
     int32_t last_variant;          /* enum ar_variant the last fused launch used (0: none yet) */
-    int32_t pad0;
+    int32_t last_cluster;          /* CTAs per row of that launch (1: no cluster; 0: none yet) */
 } ar_fusion_ws_info;
 
 /* Device-resident state (the page's 5-int flag array, widened).  Read it with
@@ -238,9 +238,11 @@ int ar_fusion_workspace_set_mode(ar_fusion_ws* ws, int mode);
  * call).  cluster_size: CTAs per token row for the one-row-per-block kernel
  * (TensorRT-LLM allReduceFusionKernels.cu, allreduce_fusion_kernel_launcher
  * splits a token over a thread-block cluster and combines the sum of squares
- * through distributed shared memory, rms_norm): 0 = automatic, 1 = no
- * cluster, 2, 4 or 8; used only where a row still has at least one 16-byte
- * vector per thread.  pdl: 1 = programmatic dependent launch (the same
+ * through distributed shared memory, rms_norm): 0 = automatic (2 for fp32
+ * rows of 4097..8192 elements with more than 4 ranks and at least 256
+ * tokens, where it measured faster; else 1), 1 = no cluster, 2, 4 or 8;
+ * used only where each CTA of the cluster still holds one vector (8
+ * elements) per thread.  pdl: 1 = programmatic dependent launch (the same
  * launcher's programmaticStreamSerialization attribute): the fused kernel
  * may be scheduled while the preceding kernel on the stream finishes and
  * waits on the device for its results.  Errors: AR_ERR_INVALID. */

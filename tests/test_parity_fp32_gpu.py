@@ -149,3 +149,23 @@ def test_fp32_vector_sum(R, N, offset):
     B.ar_fusion_sum_ex([dev[r, offset:] for r in range(R)], out[offset:], B.AR_ACC_ELEMENT, n=N)
     torch.cuda.synchronize()
     assert np.array_equal(out[offset:].cpu().numpy().view(np.uint32), exp.view(np.uint32))
+
+
+@pytest.mark.parametrize("R,T,H,dtype,expect", [(8, 256, 7168, "fp32", 2), (16, 300, 8192, "fp32", 2),
+                                                (4, 256, 7168, "fp32", 1), (8, 128, 7168, "fp32", 1),
+                                                (8, 256, 4096, "fp32", 1), (8, 256, 7168, "bf16", 1)])
+def test_automatic_cluster_choice(R, T, H, dtype, expect):
+    # cluster 0 (automatic): fp32 rows of 513..1024 vectors with more than 4
+    # ranks and at least 256 tokens are split over 2 CTAs; results unchanged
+    w = W.FusedWorkload(f"auto_cluster_{R}_{T}_{H}_{dtype}", R=R, T=T, H=H, dtype=dtype,
+                        pattern=W.RES_NORM_NVFP4, seed=T + R)
+    inp = W.make_fused_inputs(w)
+    ws = make_ws(w)
+    exp = PY.oracle_expected(w, inp)
+    got = PY.run_gpu(ws, w, inp, scale=exp["scale"])
+    stats = PY.check_all(w, got, exp)
+    assert stats["residual_mismatch"] == 0, stats
+    info = B.ar_fusion_workspace_info(ws)
+    assert info["last_variant"] == B.AR_VARIANT_CTA_ROW
+    assert info["last_cluster"] == expect
+    B.ar_fusion_workspace_destroy(ws)
