@@ -29,10 +29,15 @@
  *           NaN = S.1111.111, largest finite 448, subnormal step 2^-9
  *   e2m1  : OCP FP4: 1/2/1, bias 1, values {0,.5,1,1.5,2,3,4,6}, no inf/NaN
  *
+ * Element types: bf16 / fp16 arrays are handled as uint16 bit patterns; the
+ * *_f32 functions take float arrays (FlashInfer's use_fp32_lamport exchange
+ * type), where every rounding to the element type is the identity.
+ *
  * Parity pins for every function live in tests/test_oracle_*.py.  The NVFP4
- * scale-factor layout and global-scale convention are a stated reading (the
- * quantiser's helper header is not on the pages): parity unpinned for those two
- * conventions only.
+ * global-scale convention (gs = 2688 / amax, enc = gs / f(sf)) is a stated
+ * reading (the quantiser's helper header is not on the pages): parity
+ * unpinned for that convention only.  The block-scale tile layout is pinned
+ * outside the oracle, by a block-scaled matmul library reading it.
  */
 #include <math.h>
 #include <stdint.h>
