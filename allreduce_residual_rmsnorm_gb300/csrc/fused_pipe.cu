@@ -5,14 +5,15 @@
 // the bytes move differently:
 //
 //   * persistent blocks, one per SM, rows strided over the grid;
-//   * one producer lane streams every input row of its rows -- the R rank
-//     partials, then the residual -- into a ring of S shared-memory stages
-//     with 1-D bulk async copies (cp.async.bulk, the TMA engine) that signal
-//     an mbarrier per stage ("full") with their byte count;
+//   * one producer lane streams the input rows of its rows in slice groups
+//     (at most 2 x NC vectors of one source row; the R rank partials of a
+//     group, then the residual's) into a ring of S shared-memory stages with
+//     1-D bulk async copies (cp.async.bulk, the TMA engine) that signal an
+//     mbarrier per stage ("full") with their byte count;
 //   * consumer warps wait on "full", fold the stage into fp32 accumulators
 //     held in registers (rank order, as the oracle), and release the stage
 //     ("empty", one arrival per consumer warp);
-//   * so the copy engine keeps up to S row-sized transfers in flight per SM
+//   * so the copy engine keeps up to S transfers in flight per SM
 //     while the consumers reduce, normalise, quantise and store the previous
 //     row -- memory-level parallelism without registers.
 //
@@ -107,17 +108,37 @@ struct Ring {
     }
 };
 
+// Stage = one "slice group" of one source row: KPS consecutive k-slices, where
+// k-slice k holds vectors [k * NC, (k + 1) * NC) -- one vector per consumer
+// thread.  Stages of a row come in the order (group j, source u): the R rank
+// partials of group j, then its residual, then group j + 1.  A consumer
+// therefore finishes the rank sum of KPS vectors before the next group
+// arrives and keeps only the packed y of the row in registers; and a stage is
+// at most KPS * NC vectors (16 KB of bf16 at NC = 512) whatever the hidden
+// size, so the ring holds ~10 copies in flight even for 32768-wide rows.
+template <int VPT>
+__host__ __device__ constexpr int pipe_kps()
+{
+    return VPT < 2 ? VPT : 2;
+}
+
 template <class D, int VPT>
 __global__ void __launch_bounds__(544, 1)
 fused_pipe_kernel(const FusedArgs a, const int S, const int NC)
 {
+    using V = typename D::Vec;
+    constexpr int EB = D::bytes;
+    constexpr int VB = 8 * EB;
+    constexpr int KPS = pipe_kps<VPT>();
+    constexpr int NG = VPT / KPS;           // slice groups per row
     extern __shared__ __align__(1024) uint8_t smem[];
     const int H = a.H;
     const int Hv = H >> 3;
     const int R = a.R;
     const int pat = a.pattern;
-    const uint32_t stage_bytes = (uint32_t)H * 2;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * stage_bytes);
+    const uint32_t row_bytes = (uint32_t)H * EB;
+    const uint32_t group_bytes = (uint32_t)(KPS * NC * VB);   // stage capacity
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * group_bytes);
     uint64_t* empty = full + kMaxStages;
     DF* red = reinterpret_cast<DF*>(empty + kMaxStages);   // [2][32]
     float* rstd_sh = reinterpret_cast<float*>(red + 64);   // [2]
@@ -148,24 +169,30 @@ fused_pipe_kernel(const FusedArgs a, const int S, const int NC)
             uint32_t issued = 0;
             bool ok = true;
             for (int row = blockIdx.x; ok && row < a.T; row += gridDim.x) {
-                const size_t roff = (size_t)row * stage_bytes;
-                for (int u = 0; u <= R; ++u) {
-                    // a stage's previous use must have been released by every consumer warp
-                    if (issued >= (uint32_t)S && !mbar_wait(empty0 + 8u * ring.s, ring.ph ^ 1u, tmo)) {
-                        record_error(a.state, AR_ERR_TIMEOUT, -2);
-                        *abort_flag = 1;
-                        ok = false;
-                        break;
+                const size_t roff = (size_t)row * row_bytes;
+                for (int j = 0; ok && j < NG; ++j) {
+                    // bytes of group j inside the row (every group holds at least
+                    // one vector: checked at launch)
+                    const uint32_t goff = (uint32_t)j * group_bytes;
+                    const uint32_t gb = row_bytes - goff < group_bytes ? row_bytes - goff : group_bytes;
+                    for (int u = 0; u <= R; ++u) {
+                        // a stage's previous use must have been released by every consumer warp
+                        if (issued >= (uint32_t)S && !mbar_wait(empty0 + 8u * ring.s, ring.ph ^ 1u, tmo)) {
+                            record_error(a.state, AR_ERR_TIMEOUT, -2);
+                            *abort_flag = 1;
+                            ok = false;
+                            break;
+                        }
+                        if (*abort_flag) {
+                            ok = false;
+                            break;
+                        }
+                        const uint8_t* src = (u < R ? a.partial[u] : a.residual_in) + roff + goff;
+                        mbar_arrive_expect_tx(full0 + 8u * ring.s, gb);
+                        bulk_g2s(smem0 + ring.s * group_bytes, src, gb, full0 + 8u * ring.s);
+                        ++issued;
+                        ring.next((uint32_t)S);
                     }
-                    if (*abort_flag) {
-                        ok = false;
-                        break;
-                    }
-                    const uint8_t* src = u < R ? a.partial[u] + roff : a.residual_in + roff;
-                    mbar_arrive_expect_tx(full0 + 8u * ring.s, stage_bytes);
-                    bulk_g2s(smem0 + ring.s * stage_bytes, src, stage_bytes, full0 + 8u * ring.s);
-                    ++issued;
-                    ring.next((uint32_t)S);
                 }
             }
             // tail: every issued copy must have landed before the block may exit
@@ -198,55 +225,56 @@ fused_pipe_kernel(const FusedArgs a, const int S, const int NC)
     Ring ring;
     int parity = 0;
     for (int row = blockIdx.x; row < a.T; row += gridDim.x) {
-        const size_t roff = (size_t)row * stage_bytes;
-        float acc[VPT][8];
-        uint4 xr[VPT];
-        bool ok = true;
-        for (int u = 0; u <= R; ++u) {
-            if (!mbar_wait(full0 + 8u * ring.s, ring.ph, tmo)) {
-                record_error(a.state, AR_ERR_TIMEOUT, -1);
-                *abort_flag = 1;
-                ok = false;
-                break;
-            }
-            const uint8_t* st = smem + (size_t)ring.s * stage_bytes;
-            uint4 w[VPT];
-#pragma unroll
-            for (int k = 0; k < VPT; ++k) {
-                const int v = g + k * NC;
-                w[k] = v < Hv ? *reinterpret_cast<const uint4*>(st + (size_t)v * 16)
-                              : make_uint4(0, 0, 0, 0);
-            }
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(empty0 + 8u * ring.s);
-            ring.next((uint32_t)S);
-#pragma unroll
-            for (int k = 0; k < VPT; ++k) {
-                if (u == 0)
-                    unpack8<D>(w[k], acc[k]);
-                else if (u < R) {
-                    add8<D>(acc[k], w[k]);
-                    if (a.acc)
-                        round8<D>(acc[k]);
-                }
-                else
-                    xr[k] = w[k];
-            }
-        }
-
+        const size_t roff = (size_t)row * row_bytes;
         DF ss = {0.0f, 0.0f};
-        uint4 yv[VPT];
-        if (ok) {
+        V yv[VPT];
+        bool ok = true;
 #pragma unroll
-            for (int k = 0; k < VPT; ++k) {
+        for (int j = 0; j < NG; ++j) {
+            float acc[KPS][8];
+            V xr[KPS];
+            for (int u = 0; ok && u <= R; ++u) {
+                if (!mbar_wait(full0 + 8u * ring.s, ring.ph, tmo)) {
+                    record_error(a.state, AR_ERR_TIMEOUT, -1);
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+                const uint8_t* st = smem + (size_t)ring.s * group_bytes;
+                V w[KPS];
+#pragma unroll
+                for (int kk = 0; kk < KPS; ++kk) {
+                    const int v = g + (j * KPS + kk) * NC;
+                    w[kk] = v < Hv ? *reinterpret_cast<const V*>(st + (size_t)(g + kk * NC) * VB)
+                                   : zero_vec<V>();
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(empty0 + 8u * ring.s);
+                ring.next((uint32_t)S);
+#pragma unroll
+                for (int kk = 0; kk < KPS; ++kk) {
+                    if (u == 0)
+                        unpack8<D>(w[kk], acc[kk]);
+                    else if (u < R) {
+                        add8<D>(acc[kk], w[kk]);
+                        if (a.acc)
+                            round8<D>(acc[kk]);
+                    }
+                    else
+                        xr[kk] = w[kk];
+                }
+            }
+#pragma unroll
+            for (int kk = 0; kk < KPS; ++kk) {
+                const int k = j * KPS + kk;
                 const int v = g + k * NC;
-                if (v < Hv) {
-                    yv[k] = residual_vec<D>(acc[k], xr[k], ss);
+                if (ok && v < Hv) {
+                    yv[k] = residual_vec<D>(acc[kk], xr[kk], ss);
                     if (pat & AR_RESIDUAL_OUT)
-                        st_vec(a.residual_out + roff + (size_t)v * 16, yv[k]);
+                        st_vec(a.residual_out + roff + (size_t)v * VB, yv[k]);
                 } else {
-                    yv[k] = make_uint4(0, 0, 0, 0);
+                    yv[k] = zero_vec<V>();
                 }
             }
         }
@@ -300,7 +328,11 @@ cudaError_t launch_t(const FusedArgs& a, const LaunchCfg& c)
     if (!fn)
         return cudaErrorInvalidValue;
     const int NC = ((Hv + vpt - 1) / vpt + 31) / 32 * 32;
-    const uint32_t stage_bytes = (uint32_t)a.H * 2;
+    const int kps = vpt < 2 ? vpt : 2;
+    // every slice group must hold at least one vector of the row
+    if (NC * (vpt - kps) >= Hv)
+        return cudaErrorInvalidValue;
+    const uint32_t stage_bytes = (uint32_t)(kps * NC * 8 * D::bytes);
     // ring depth: ~160 KB of copies in flight per SM (a sweep at H = 7168 was
     // flat from 10 to 12 stages and lost bandwidth above 16 and below 8)
     int S = (int)(kRingTarget / stage_bytes);
@@ -315,7 +347,7 @@ cudaError_t launch_t(const FusedArgs& a, const LaunchCfg& c)
         return cudaErrorInvalidValue;
     const uint32_t smem = (uint32_t)S * stage_bytes + kSmemTail;
     static std::mutex mu;
-    static bool attr_set[2][9] = {};
+    static bool attr_set[3][9] = {};
     {
         std::lock_guard<std::mutex> lk(mu);
         if (!attr_set[D::id][vpt]) {
@@ -336,17 +368,21 @@ cudaError_t launch_t(const FusedArgs& a, const LaunchCfg& c)
 
 }  // namespace
 
-// bf16 / fp16 only: fp32 rows take the register-resident row kernels
 bool fused_pipe_supported(int dtype, int H, int R)
 {
-    return (dtype == AR_DT_BF16 || dtype == AR_DT_FP16) && H % 8 == 0 && H <= AR_MAX_HIDDEN && R >= 1 && R <= AR_MAX_RANKS;
+    return dtype_supported(dtype) && H % 8 == 0 && H <= AR_MAX_HIDDEN && R >= 1 && R <= AR_MAX_RANKS;
 }
 
 cudaError_t launch_fused_pipe(int dtype, const FusedArgs& a, const LaunchCfg& c)
 {
     if (a.lamport || a.amax_out || !fused_pipe_supported(dtype, a.H, a.R))
         return cudaErrorNotSupported;
-    return dtype == AR_DT_BF16 ? launch_t<Bf16>(a, c) : launch_t<Fp16>(a, c);
+    switch (dtype) {
+    case AR_DT_BF16: return launch_t<Bf16>(a, c);
+    case AR_DT_FP16: return launch_t<Fp16>(a, c);
+    case AR_DT_FP32: return launch_t<F32>(a, c);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace arf

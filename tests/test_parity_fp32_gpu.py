@@ -35,8 +35,8 @@ def test_fp32_decode_r8_t128_h4096(staged):
 @pytest.mark.parametrize("variant,staged", [(B.AR_VARIANT_AUTO, True), (B.AR_VARIANT_CTA_ROW, False),
                                             (B.AR_VARIANT_BULK_PIPE, False)])
 def test_fp32_prefill_r8_t1024_h7168_nvfp4(variant, staged):
-    # hidden 7168 = 896 vectors of 8 fp32: two vectors per thread; the bulk
-    # pipeline takes 16-bit rows only, so that request runs the row kernel
+    # hidden 7168 = 896 vectors of 8 fp32: AUTO splits the row over a 2-CTA
+    # cluster; the row kernel alone takes two vectors per thread
     w = W.FP32_PREFILL
     stats, _, _ = run_and_check(w, variant, staged)
     assert stats["residual_mismatch"] == 0, stats
@@ -54,7 +54,8 @@ EDGE32 = [
 
 
 @pytest.mark.parametrize("R,T,H,pattern", EDGE32)
-@pytest.mark.parametrize("variant", [B.AR_VARIANT_AUTO, B.AR_VARIANT_WARP_ROW, B.AR_VARIANT_CTA_ROW])
+@pytest.mark.parametrize("variant", [B.AR_VARIANT_AUTO, B.AR_VARIANT_WARP_ROW, B.AR_VARIANT_CTA_ROW,
+                                     B.AR_VARIANT_BULK_PIPE])
 def test_fp32_edge_shapes(R, T, H, pattern, variant):
     w = W.FusedWorkload(f"edge32_{R}_{T}_{H}", R=R, T=T, H=H, dtype="fp32", pattern=pattern,
                         eps=1e-5, seed=R * 1000 + T + 7)
