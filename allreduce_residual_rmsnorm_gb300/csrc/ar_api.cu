@@ -330,29 +330,41 @@ int pick_variant(const ar_fusion_ws* ws, const FusedArgs& a)
         v = AR_VARIANT_AUTO;
     if (v != AR_VARIANT_AUTO)
         return v;
-    // measured at R = 8, T = 8192, H = 7168: one-row-per-block with one
-    // vector per thread beats the bulk-copy pipeline (184-188 us vs 210 us);
-    // one row per warp only up to hidden 512 (at hidden 1024 the block
-    // version is faster: 131.5 vs 156.5 us at 32768 tokens)
-    return a.H <= 512 ? AR_VARIANT_WARP_ROW : AR_VARIANT_CTA_ROW;
+    // One row per warp only up to hidden 512 (at hidden 1024 the block
+    // version is faster: 131.5 vs 156.5 us at 32768 tokens).
+    if (a.H <= 512)
+        return AR_VARIANT_WARP_ROW;
+    // Rows that fit one vector per thread of a row block, with at most 8
+    // ranks, stay on the register-resident kernel (R = 8, T = 8192, H = 7168:
+    // 180-186 us vs 193-214 us for the pipe).  Wider rows (several vectors per
+    // thread), and more than 8 ranks of rows over 8 KB, move to the bulk-copy
+    // pipe once the inputs exceed ~L2 (96 MiB): bf16 R = 8, H = 16384,
+    // T = 4096: 223.8 vs 297.2 us; H = 32768: 260.9 vs 344.9 us; bf16 R = 16,
+    // H = 8192: 192.2 vs 240.0 us; R = 12, H = 7168: 135.1 vs 146.6 us; fp32
+    // R = 16, H = 4096: 192.5 vs 252.1 us.  Rows of 8 KB or less make stages
+    // too small for the pipe (bf16 R = 16, H = 4096: 121.4 vs 103.3 us;
+    // H = 1024: 392 vs 102 us), and below ~L2 the row kernel's L2 hits win
+    // (fp32 R = 8, H = 7168, T = 304: 11.2 vs 15.2 us).
+    const int Hv = a.H / 8;
+    const uint64_t eb = (uint64_t)elem_bytes(ws->dtype);
+    const uint64_t in_bytes = (uint64_t)(a.R + 1) * a.T * a.H * eb;
+    const bool wide = Hv > one_vec_threads_for((int)eb, a.R);
+    const bool many_ranks = a.R > 8 && (uint64_t)a.H * eb > 8192;
+    if (!a.lamport && !a.amax_out && in_bytes >= (96ull << 20) && (wide || many_ranks) &&
+        fused_pipe_supported(ws->dtype, a.H, a.R))
+        return AR_VARIANT_BULK_PIPE;
+    return AR_VARIANT_CTA_ROW;
 }
 
-// CTAs per row when the caller left the choice to the library (cluster 0).
-// fp32 rows of more than 512 vectors (hidden > 4096) would need two vectors
-// per thread in one CTA; with more than 4 ranks, splitting each row over a
-// cluster of 2 CTAs (one vector per thread) is faster: at R = 8, H = 7168,
-// 391.0 vs 494.4 us (8192 tokens) and 60.6 vs 70.0 us (1024 tokens).  With 4
-// ranks (H = 8192: 88.1 vs 80.8 us) and for every bf16 / fp16 case measured
-// (e.g. R = 8, T = 8192, H = 7168: 231.8 vs 180.1 us) one CTA per row wins.
-int auto_cluster(const ar_fusion_ws* ws, const FusedArgs& a, int variant)
+// CTAs per row when the caller left the choice to the library (cluster 0):
+// one.  A cluster split measured slower wherever the row kernel is used by
+// default: decode sizes (R = 8, T = 128, H = 4096: 7.65 vs 7.09 us), bf16
+// prefill (R = 8, T = 8192, H = 7168: 231.8 vs 180.1 us), and the wide rows
+// that it helps (fp32 R = 8, H = 7168: 391.0 vs 494.4 us at 8192 tokens) run
+// on the bulk-copy pipe instead (229 us).
+int auto_cluster(const ar_fusion_ws* ws)
 {
-    if (ws->cluster > 0)
-        return ws->cluster;
-    const int Hv = a.H / 8;
-    if (ws->dtype == AR_DT_FP32 && variant == AR_VARIANT_CTA_ROW && a.R > 4 && Hv > 512 &&
-        Hv <= 1024 && a.T >= 256)
-        return 2;
-    return 1;
+    return ws->cluster > 0 ? ws->cluster : 1;
 }
 
 int launch_fused(ar_fusion_ws* ws, const FusedArgs& a, cudaStream_t s)
@@ -360,7 +372,7 @@ int launch_fused(ar_fusion_ws* ws, const FusedArgs& a, cudaStream_t s)
     LaunchCfg c{ws->sms, s};
     c.pdl = ws->pdl;
     const int variant = pick_variant(ws, a);
-    c.cluster = auto_cluster(ws, a, variant);
+    c.cluster = auto_cluster(ws);
     ws->last_variant = variant;
     ws->last_cluster = 1;
     c.used_cluster = &ws->last_cluster;

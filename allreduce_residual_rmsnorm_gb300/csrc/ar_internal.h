@@ -66,6 +66,15 @@ inline bool vec_aligned(const void* p, int dtype)
     return ((uintptr_t)p & (dtype == AR_DT_FP32 ? 31u : 15u)) == 0;
 }
 
+// Threads of a one-vector-per-thread row block (one row per block): bf16 /
+// fp16 up to 896 (72 registers each) with up to 8 ranks, 1024 (64 registers)
+// with up to 4; fp32 vectors take twice the registers: up to 512.  Rows of
+// more vectors take several vectors per thread.
+__host__ __device__ constexpr int one_vec_threads_for(int elem_bytes, int nranks)
+{
+    return elem_bytes == 4 ? 512 : (nranks <= 4 ? 1024 : 896);
+}
+
 // Record `msg` as the calling thread's ar_fusion_last_error() text; returns code.
 int set_last_error(int code, const char* msg);
 

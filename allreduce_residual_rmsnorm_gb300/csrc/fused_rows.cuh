@@ -28,13 +28,11 @@
 
 namespace arf {
 
-// Threads of a one-vector-per-thread row block: bf16 / fp16 up to 896 (72
-// registers each) with up to 8 ranks, 1024 (64 registers) with up to 4; fp32
-// vectors take twice the registers: up to 512.
+// Threads of a one-vector-per-thread row block (one_vec_threads_for).
 template <class D>
 __host__ __device__ constexpr int one_vec_threads(int rmax)
 {
-    return D::bytes == 4 ? 512 : (rmax <= 4 ? 1024 : 896);
+    return one_vec_threads_for(D::bytes, rmax);
 }
 
 // Block size bound: one_vec_threads for one vector per thread; wider rows

@@ -311,13 +311,16 @@ def run_sweep(args):
     def cold_us(body):
         return graph_us(lambda: (flush(), body())) - graph_us(flush)
 
-    def report(w, pat, ws, lam, us, cl, pdl):
-        rc, _ = B.ar_fusion_workspace_status(ws)
+    def fused_bytes(w, pat):
         eb = 4 if w.dtype == "fp32" else 2
         outb = (w.T * w.H * eb if pat & B.AR_NORM_OUT else 0) + \
                (w.T * w.H if pat & B.AR_QUANT_FP8 else 0) + \
                (w.T * w.H // 2 + w.T * w.H // 16 if pat & B.AR_QUANT_NVFP4 else 0)
-        byts = w.R * w.T * w.H * eb + w.T * w.H * eb * (2 if pat & B.AR_RESIDUAL_OUT else 1) + outb
+        return w.R * w.T * w.H * eb + w.T * w.H * eb * (2 if pat & B.AR_RESIDUAL_OUT else 1) + outb
+
+    def report(w, pat, ws, lam, us, cl, pdl):
+        rc, _ = B.ar_fusion_workspace_status(ws)
+        byts = fused_bytes(w, pat)
         info = B.ar_fusion_workspace_info(ws)
         last = info["last_variant"]
         print(json.dumps({"sweep": w.name, "dtype": w.dtype, "mode": "lamport" if lam else "buffer",
@@ -378,8 +381,11 @@ def run_sweep(args):
             us = cold_us(lambda: B.ar_fusion_run(ws, parts, X, G, w.eps, pat, out["res"],
                                                  out["norm"], q, sf, sc))
             rc, _ = B.ar_fusion_workspace_status(ws)
+            byts = fused_bytes(w, pat)
             print(json.dumps({"sweep": w.name, "dtype": w.dtype, "mode": "caller partials",
-                              "us": us, "tokens_per_s": w.T / (us * 1e-6),
+                              "us": us, "tokens_per_s": w.T / (us * 1e-6), "bytes": byts,
+                              "gbs": byts / (us * 1e-6) / 1e9,
+                              "frac_of_copy_peak": byts / (us * 1e-6) / 1e9 / peak,
                               "l2": f"cold: {3 * l2_bytes / 1e6:.0f} MB read between calls",
                               "status": rc}), flush=True)
         B.ar_fusion_workspace_destroy(ws)
@@ -396,6 +402,7 @@ def run_sweep(args):
             uc = cold_us(lambda: B.ar_fusion_sum(bufs, out))
             print(json.dumps({"sweep": sw.name, "dtype": sw.dtype, "us": uc, "bytes": byts,
                               "gbs": byts / (uc * 1e-6) / 1e9,
+                              "frac_of_copy_peak": byts / (uc * 1e-6) / 1e9 / peak,
                               "l2": f"cold: {3 * l2_bytes / 1e6:.0f} MB read between calls"}),
                   flush=True)
         print(json.dumps({"sweep": sw.name, "dtype": sw.dtype, "us": us, "bytes": byts,

@@ -116,7 +116,12 @@ enum ar_mode {
     AR_MODE_BUFFER = 2        /* the buffer region, rank r at r * max_token_num * hidden */
 };
 
-/* Kernel variant (normally chosen by hidden size and token count). */
+/* Kernel variant.  AUTO: one row per warp for hidden <= 512; the bulk-copy
+ * pipe for inputs ((nranks + 1) * tokens * hidden elements) of at least
+ * 96 MiB outside Lamport mode when a row needs more than one vector of 8
+ * elements per thread of a row block (hidden > 7168 bf16/fp16 with more than
+ * 4 ranks, > 8192 with up to 4, > 4096 fp32), or nranks > 8 with rows of
+ * more than 8 KB; else one row per thread block. */
 enum ar_variant {
     AR_VARIANT_AUTO = 0,
     AR_VARIANT_WARP_ROW = 1,  /* one row per warp (small hidden) */
@@ -238,9 +243,9 @@ int ar_fusion_workspace_set_mode(ar_fusion_ws* ws, int mode);
  * call).  cluster_size: CTAs per token row for the one-row-per-block kernel
  * (TensorRT-LLM allReduceFusionKernels.cu, allreduce_fusion_kernel_launcher
  * splits a token over a thread-block cluster and combines the sum of squares
- * through distributed shared memory, rms_norm): 0 = automatic (2 for fp32
- * rows of 4097..8192 elements with more than 4 ranks and at least 256
- * tokens, where it measured faster; else 1), 1 = no cluster, 2, 4 or 8;
+ * through distributed shared memory, rms_norm): 0 = automatic (one CTA per
+ * row: the split measured slower wherever the library picks the row
+ * kernel), 1 = no cluster, 2, 4 or 8;
  * used only where each CTA of the cluster still holds one vector (8
  * elements) per thread.  pdl: 1 = programmatic dependent launch (the same
  * launcher's programmaticStreamSerialization attribute): the fused kernel

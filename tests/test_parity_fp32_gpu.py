@@ -152,13 +152,19 @@ def test_fp32_vector_sum(R, N, offset):
     assert np.array_equal(out[offset:].cpu().numpy().view(np.uint32), exp.view(np.uint32))
 
 
-@pytest.mark.parametrize("R,T,H,dtype,expect", [(8, 256, 7168, "fp32", 2), (16, 300, 8192, "fp32", 2),
-                                                (4, 256, 7168, "fp32", 1), (8, 128, 7168, "fp32", 1),
-                                                (8, 256, 4096, "fp32", 1), (8, 256, 7168, "bf16", 1)])
-def test_automatic_cluster_choice(R, T, H, dtype, expect):
-    # cluster 0 (automatic): fp32 rows of 513..1024 vectors with more than 4
-    # ranks and at least 256 tokens are split over 2 CTAs; results unchanged
-    w = W.FusedWorkload(f"auto_cluster_{R}_{T}_{H}_{dtype}", R=R, T=T, H=H, dtype=dtype,
+@pytest.mark.parametrize("R,T,H,dtype,expect", [
+    (8, 512, 16384, "bf16", B.AR_VARIANT_BULK_PIPE),    # two vectors per thread, 151 MB of inputs
+    (16, 450, 7168, "bf16", B.AR_VARIANT_BULK_PIPE),    # 16 ranks of 14 KB rows, 110 MB
+    (16, 400, 7168, "bf16", B.AR_VARIANT_CTA_ROW),      # 97.5 MB: below the 96 MiB threshold
+    (16, 1024, 4096, "bf16", B.AR_VARIANT_CTA_ROW),     # 16 ranks of 8 KB rows
+    (8, 1024, 7168, "bf16", B.AR_VARIANT_CTA_ROW),      # one vector per thread, 8 ranks
+    (8, 512, 7168, "fp32", B.AR_VARIANT_BULK_PIPE),     # fp32: 896 vectors > 512 threads
+    (8, 256, 7168, "fp32", B.AR_VARIANT_CTA_ROW),       # 66 MB
+    (16, 512, 4096, "fp32", B.AR_VARIANT_BULK_PIPE),    # 16 ranks of 16 KB rows
+    (4, 2048, 512, "bf16", B.AR_VARIANT_WARP_ROW),
+])
+def test_automatic_variant_choice(R, T, H, dtype, expect):
+    w = W.FusedWorkload(f"auto_{R}_{T}_{H}_{dtype}", R=R, T=T, H=H, dtype=dtype,
                         pattern=W.RES_NORM_NVFP4, seed=T + R)
     inp = W.make_fused_inputs(w)
     ws = make_ws(w)
@@ -167,6 +173,6 @@ def test_automatic_cluster_choice(R, T, H, dtype, expect):
     stats = PY.check_all(w, got, exp)
     assert stats["residual_mismatch"] == 0, stats
     info = B.ar_fusion_workspace_info(ws)
-    assert info["last_variant"] == B.AR_VARIANT_CTA_ROW
-    assert info["last_cluster"] == expect
+    assert info["last_variant"] == expect
+    assert info["last_cluster"] == 1
     B.ar_fusion_workspace_destroy(ws)
