@@ -33,7 +33,7 @@ def main(argv=None):
     p.add_argument("--tokens", type=int, default=2048)
     p.add_argument("--hidden", type=int, default=7168)
     p.add_argument("--pattern", default="res_nvfp4", choices=sorted(B.PATTERNS))
-    p.add_argument("--dtype", default="bf16", choices=["bf16", "fp16"])
+    p.add_argument("--dtype", default="bf16", choices=["bf16", "fp16", "fp32"])
     p.add_argument("--cluster", type=int, default=0)
     p.add_argument("--pdl", type=int, default=0)
     p.add_argument("--lamport", action="store_true")
@@ -60,7 +60,7 @@ def main(argv=None):
     w = W.FusedWorkload("case", R=a.ranks, T=a.tokens, H=a.hidden, dtype=a.dtype,
                         pattern=a.pattern, heavy_frac=0.01)
     inp = W.make_fused_inputs(w)
-    dt = B.AR_DT_BF16 if a.dtype == "bf16" else B.AR_DT_FP16
+    dt = {"bf16": B.AR_DT_BF16, "fp16": B.AR_DT_FP16, "fp32": B.AR_DT_FP32}[a.dtype]
     P, X, G = inp.partials.to(dev), inp.residual.to(dev), inp.gamma.to(dev)
     ws = B.ar_fusion_workspace_create(w.R, w.T, w.H, dt)
     B.ar_fusion_workspace_set_variant(ws, {"auto": B.AR_VARIANT_AUTO, "warp": B.AR_VARIANT_WARP_ROW,
