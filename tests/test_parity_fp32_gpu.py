@@ -176,3 +176,28 @@ def test_automatic_variant_choice(R, T, H, dtype, expect):
     assert info["last_variant"] == expect
     assert info["last_cluster"] == 1
     B.ar_fusion_workspace_destroy(ws)
+
+
+def test_fp32_norm_amax_matches_oracle():
+    w = W.FusedWorkload("fp32_amax", R=4, T=96, H=2048, dtype="fp32", heavy_frac=0.01, seed=21,
+                        pattern=W.RES_NORM_FP8)
+    inp = W.make_fused_inputs(w)
+    exp = PY.oracle_expected(w, inp)
+    ws = make_ws(w)
+    P = inp.partials.cuda()
+    amax = torch.full((1,), -1.0, device="cuda")
+    B.ar_fusion_norm_amax(ws, [P[r] for r in range(w.R)], inp.residual.cuda(), inp.gamma.cuda(),
+                          w.eps, amax)
+    torch.cuda.synchronize()
+    assert float(amax.item()) == exp["amax"]
+    B.ar_fusion_workspace_destroy(ws)
+
+
+@pytest.mark.parametrize("variant", [B.AR_VARIANT_CTA_ROW, B.AR_VARIANT_BULK_PIPE])
+def test_fp32_nvfp4_swizzled_scale_layout(variant):
+    from test_parity_gpu import _run_nvfp4_swizzled
+    w = W.FusedWorkload("fp32_swz", R=4, T=200, H=4096, dtype="fp32", pattern=W.RES_NORM_NVFP4,
+                        heavy_frac=0.01, seed=33)
+    exp, q, sf = _run_nvfp4_swizzled(w, variant)
+    PY.assert_codes(q.cpu().numpy(), exp["quant"], "e2m1", "fp4 codes")
+    PY.assert_codes(sf.cpu().numpy(), oracle.swizzle_scales(exp["sf"]), "e4m3", "swizzled scales")
