@@ -162,6 +162,36 @@ __device__ __forceinline__ void add8(float (&s)[8], const typename D::Vec& v)
     }
 }
 
+// rnd(f(a) + f(b)) for two packed 16-bit vectors, one packed add per pair:
+// the fp32 sum of two bf16 (fp16) values rounded once more to bf16 (fp16)
+// equals the correctly rounded sum (when the exact sum is not an fp32 value
+// the smaller addend lies at least 16 (13) bits below the larger one's last
+// bit, so the fp32 rounding cannot land on a 16-bit tie).
+template <class D>
+__device__ __forceinline__ uint4 add_packed(const uint4& a, const uint4& b);
+
+template <>
+__device__ __forceinline__ uint4 add_packed<Bf16>(const uint4& a, const uint4& b)
+{
+    uint4 r;
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r.x) : "r"(a.x), "r"(b.x));
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r.y) : "r"(a.y), "r"(b.y));
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r.z) : "r"(a.z), "r"(b.z));
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r.w) : "r"(a.w), "r"(b.w));
+    return r;
+}
+
+template <>
+__device__ __forceinline__ uint4 add_packed<Fp16>(const uint4& a, const uint4& b)
+{
+    uint4 r;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r.x) : "r"(a.x), "r"(b.x));
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r.y) : "r"(a.y), "r"(b.y));
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r.z) : "r"(a.z), "r"(b.z));
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r.w) : "r"(a.w), "r"(b.w));
+    return r;
+}
+
 // s[i] = f(rnd(s[i])): the element-type accumulation rounds every partial sum
 // (nothing to do for fp32 elements)
 template <class D>
@@ -436,6 +466,20 @@ __host__ __device__ __forceinline__ void df_add_term(DF& a, float t)
 {
     float s, err;
     two_sum(a.hi, t, s, err);
+    a.hi = s;
+    a.lo = rn_add(a.lo, err);
+}
+
+// df_add_term for a non-negative running sum and term (sums of squares):
+// ordering the two by max / min makes Dekker's fast two-sum exact, one
+// operation fewer than TwoSum.  The new high part is still hi + t itself, so
+// a NaN term propagates as before.
+__host__ __device__ __forceinline__ void df_add_nonneg(DF& a, float t)
+{
+    const float s = rn_add(a.hi, t);
+    const float big = fmaxf(a.hi, t);
+    const float small = fminf(a.hi, t);
+    const float err = rn_add(rn_add(big, -s), small);
     a.hi = s;
     a.lo = rn_add(a.lo, err);
 }

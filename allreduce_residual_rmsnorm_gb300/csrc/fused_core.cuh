@@ -20,19 +20,22 @@ template <class D>
 __device__ __forceinline__ typename D::Vec residual_vec(const float (&s)[8],
                                                         const typename D::Vec& x, DF& ss)
 {
-    float a[8];
-    unpack8<D>(pack8<D>(s), a);
-    add8<D>(a, x);
-    const typename D::Vec y = pack8<D>(a);
     if constexpr (D::bytes == 4) {
+        float a[8];
+        unpack8<D>(pack8<D>(s), a);
+        add8<D>(a, x);
+        const typename D::Vec y = pack8<D>(a);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const float p = __fmul_rn(a[i], a[i]);
             const float e = __fmaf_rn(a[i], a[i], -p);
-            df_add_term(ss, p);
+            df_add_nonneg(ss, p);
             ss.lo = __fadd_rn(ss.lo, e);
         }
+        return y;
     } else {
+        // a = rnd(s); y = rnd(f(a) + f(x)) by packed 16-bit adds
+        const typename D::Vec y = add_packed<D>(pack8<D>(s), x);
         float t[8];
         sq2<D>(t[0], t[1], y.x);
         sq2<D>(t[2], t[3], y.y);
@@ -40,9 +43,9 @@ __device__ __forceinline__ typename D::Vec residual_vec(const float (&s)[8],
         sq2<D>(t[6], t[7], y.w);
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-            df_add_term(ss, t[i]);
+            df_add_nonneg(ss, t[i]);
+        return y;
     }
-    return y;
 }
 
 // rstd = 1 / sqrt(ss / H + eps), each step IEEE round-to-nearest.

@@ -1,7 +1,8 @@
 // Host-side check of the double-float sum-of-squares helpers of
 // ar_common.cuh (the same source the kernels use, compiled for the CPU):
-// per-thread TwoSum accumulation followed by a butterfly of df_add, as in a
-// warp reduction, must give the exact sum of squares rounded once to fp32.
+// per-thread accumulation (TwoSum, and the fast two-sum for non-negative
+// terms) followed by a butterfly of df_add, as in a warp reduction, must give
+// the exact sum of squares rounded once to fp32.
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -26,8 +27,9 @@ int main()
     std::uniform_real_distribution<float> mag(-8.0f, 8.0f);
     std::uniform_int_distribution<int> sign(0, 1);
     int bad = 0, total = 0;
-    for (int trial = 0; trial < 400; ++trial) {
-        const int lanes = 32, per = 8 * (1 + trial % 32);  // up to 8192 terms per row
+    for (int trial = 0; trial < 800; ++trial) {
+        const bool fast = trial & 1;                         // df_add_nonneg on odd trials
+        const int lanes = 32, per = 8 * (1 + (trial / 2) % 32);  // up to 8192 terms per row
         DF acc[32];
         long double exact = 0.0L;
         for (int l = 0; l < lanes; ++l) {
@@ -38,7 +40,10 @@ int main()
                     y = -y;
                 const float t = y * y;                       // exact: 8-bit significand
                 exact += (long double)t;
-                arf::df_add_term(acc[l], t);
+                if (fast)
+                    arf::df_add_nonneg(acc[l], t);
+                else
+                    arf::df_add_term(acc[l], t);
             }
         }
         for (int m = 16; m >= 1; m >>= 1) {                  // xor butterfly
