@@ -43,6 +43,17 @@ constexpr int rows_max_threads()
     return WARP_ROW ? 256 : (VPT == 1 ? one_vec_threads<D>(RMAX) : 512);
 }
 
+// Two rows per SM: 16-bit rows of 513..1024 vectors with at most 4 ranks run
+// as blocks of <= 512 threads at two vectors per thread and one vector per
+// load batch, within 64 registers, so that two blocks (two rows) share an SM
+// and one row's reductions overlap the other's loads (the launcher picks this
+// for light rows, see launch_fused_rows_t).
+template <class D, int RMAX, int VPT, bool WARP_ROW>
+__host__ __device__ constexpr int rows_min_blocks()
+{
+    return (!WARP_ROW && D::bytes == 2 && VPT == 2 && RMAX <= 4) ? 2 : 1;
+}
+
 // s[kk] (+)= rank batch r0..r0+RB-1 of vector g + (k0 + kk) * G; ELEM rounds
 // every partial sum to the element type.
 template <class D, int KCH, int RB, bool ELEM>
@@ -73,7 +84,8 @@ __device__ __forceinline__ void fold_ranks(float (&s)[KCH][8],
 // spans its CTAs (a separate instantiation, so the common one-CTA-per-row
 // kernel carries none of the cluster code).
 template <class D, int RMAX, int VPT, bool WARP_ROW, bool CLUSTER = false>
-__global__ void __launch_bounds__(rows_max_threads<D, RMAX, VPT, WARP_ROW>())
+__global__ void __launch_bounds__(rows_max_threads<D, RMAX, VPT, WARP_ROW>(),
+                                  rows_min_blocks<D, RMAX, VPT, WARP_ROW>())
 fused_rows_kernel(const FusedArgs a)
 {
     using V = typename D::Vec;
@@ -88,8 +100,10 @@ fused_rows_kernel(const FusedArgs a)
     // ranks loaded per batch
     constexpr int RBMAX = 8;
     constexpr int RB = RMAX < RBMAX ? RMAX : RBMAX;
-    // vectors per batch
-    constexpr int KCH = (LOADS / RB) > VPT ? VPT : (LOADS / RB);
+    // vectors per batch (one in the two-rows-per-SM form)
+    constexpr int KCH = rows_min_blocks<D, RMAX, VPT, WARP_ROW>() == 2
+                            ? 1
+                            : ((LOADS / RB) > VPT ? VPT : (LOADS / RB));
     static_assert(VPT % KCH == 0, "batch must divide VPT");
     static_assert(RMAX % RB == 0, "rank batch must divide RMAX");
 
@@ -321,17 +335,19 @@ fused_rows_kernel(const FusedArgs a)
             atomicMax(reinterpret_cast<unsigned int*>(a.amax_out), __float_as_uint(amax_local));
     }
 
+    // Slot state: the last block to finish advances it.  Only the next launch
+    // reads it, and kernel completion (stream order, or griddepcontrol.wait
+    // under programmatic dependent launch) already makes every write of this
+    // grid visible there, so no fence is needed (one measured 0.2-0.4 us).
     if (a.lamport) {
         __syncthreads();
         if (threadIdx.x == 0) {
-            __threadfence();
             const unsigned prev = atomicAdd(&a.state->counter, 1u);
             if (prev == gridDim.x - 1) {
                 a.state->lamport_flag = (flag + 1u) % 3u;
                 a.state->clear_size = (uint64_t)R * a.T * H;
                 a.state->calls += 1;
                 a.state->counter = 0;
-                __threadfence();
             }
         }
     }
