@@ -196,7 +196,11 @@ fused_pipe_kernel(const FusedArgs a, const int S, const int NC)
                 }
             }
             // tail: every issued copy must have landed before the block may exit
-            // (at most one use per stage is outstanding)
+            // (at most one use per stage is outstanding).  This wait is bounded
+            // by at least 200 ms whatever the caller's timeout, so that a tiny
+            // timeout cannot end the block while copies still write its shared
+            // memory.
+            const uint64_t tail_tmo = tmo > 200000000ull ? tmo : 200000000ull;
             const uint32_t n_tail = issued < (uint32_t)S ? issued : (uint32_t)S;
             for (uint32_t k = 0; k < n_tail; ++k) {
                 // step back k+1 positions from the next free position
@@ -208,7 +212,7 @@ fused_pipe_kernel(const FusedArgs a, const int S, const int NC)
                     }
                     --s;
                 }
-                if (!mbar_wait(full0 + 8u * s, ph, tmo))
+                if (!mbar_wait(full0 + 8u * s, ph, tail_tmo))
                     record_error(a.state, AR_ERR_TIMEOUT, -3);
             }
         }

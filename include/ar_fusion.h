@@ -230,7 +230,10 @@ int ar_fusion_workspace_status(ar_fusion_ws* ws, void* stream, int* detail);
 int ar_fusion_workspace_reset(ar_fusion_ws* ws, void* stream);
 
 /* Bound, in nanoseconds, of each device-side wait of later launches
- * (default 2e9).  Host-side setting; no CUDA call. */
+ * (default 2e9): the Lamport polls and the bulk-copy pipe's stage waits.  The
+ * pipe's final wait for its own copies in flight is bounded by at least
+ * 200 ms whatever this value.  Host-side setting; no CUDA call.  Errors:
+ * AR_ERR_INVALID for 0. */
 int ar_fusion_workspace_set_timeout_ns(ar_fusion_ws* ws, uint64_t ns);
 
 /* Force a kernel variant (enum ar_variant) or staged-read mode (enum
