@@ -31,8 +31,10 @@ sys.path.insert(0, ROOT)
 METRIC = "fused AR+RMSNorm tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 # device code and launch geometry of the fused kernels: a profile of DRAM
 # traffic is only reported while these are unchanged
-KERNEL_SOURCES = ["ar_common.cuh", "fused_core.cuh", "fused_pipe.cu", "fused_rows.cuh",
-                  "fused_rows_impl.cuh"]
+# device sources of the benchmarked row kernel (fused_rows_kernel<Bf16, ...>):
+# the recorded ncu traffic is valid while these are unchanged
+KERNEL_SOURCES = ["ar_common.cuh", "ar_internal.h", "fused_core.cuh", "fused_rows.cuh",
+                  "fused_rows_impl.cuh", "fused_rows_bf16.cu"]
 FALLBACK_HBM_GBS = 6800.0
 
 
