@@ -608,7 +608,8 @@ def main():
                      "frac": achieved / peak, "traffic": profiled_traffic(kname),
                      "peak_kind": f"{peak_kind} (hbm_gbs, copy bandwidth)",
                      "algorithmic_bytes_per_launch": bytes_alg,
-                     "avg_launch_us": avg_launch_s * 1e6},
+                     "avg_launch_us": avg_launch_s * 1e6,
+                     "median_launch_us": _median(launch_ms) * 1e3},
         "e2e": ({"value": e2e_value, "unit": "tokens/s",
                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                  "pipeline": f"{nch} row chunks, H2D / compute / D2H streams"} if e2e_steps else None),
