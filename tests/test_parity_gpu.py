@@ -543,3 +543,49 @@ def test_nvfp4_swizzled_output_feeds_a_block_scaled_matmul(T):
     out = _scaled_mm_nvfp4(q, sf, torch.from_numpy(b_packed).cuda(), torch.from_numpy(b_sf).cuda())
     got = out.float().cpu().numpy()
     assert np.array_equal(got, deq.astype(np.float32))
+
+
+# ------------------------------------------------------------- CUDA graphs
+
+@pytest.mark.parametrize("pdl", [0, 1])
+def test_graph_replay_of_stage_and_run_advances_the_lamport_slots(pdl):
+    # the slot index and clear size live on the device, so a captured
+    # stage + run replays correctly: each replay reads the slot its staging
+    # filled and clears the previous one
+    w = W.DECODE.with_(T=64)
+    ws = make_ws(w)
+    B.ar_fusion_workspace_set_launch(ws, 0, pdl)
+    inp0 = W.make_fused_inputs(w)
+    P = inp0.partials.cuda()
+    X, G = inp0.residual.cuda(), inp0.gamma.cuda()
+    res, nrm = torch.empty_like(X), torch.empty_like(X)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):                 # warm-up outside the capture
+        for r in range(w.R):
+            B.ar_fusion_workspace_stage(ws, r, P[r], stream=side)
+        B.ar_fusion_run(ws, None, X, G, w.eps, B.PATTERNS[w.pattern], res, nrm, stream=side)
+    torch.cuda.synchronize()
+    calls0 = B.ar_fusion_workspace_copy_state(ws)["calls"]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        for r in range(w.R):
+            B.ar_fusion_workspace_stage(ws, r, P[r], stream=side)
+        B.ar_fusion_run(ws, None, X, G, w.eps, B.PATTERNS[w.pattern], res, nrm, stream=side)
+    for k in range(5):
+        inp = W.make_fused_inputs(w.with_(seed=500 + k))
+        P.copy_(inp.partials)
+        X.copy_(inp.residual)
+        G.copy_(inp.gamma)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        exp = PY.oracle_expected(w, inp, lamport_flip=True)
+        got = {"residual": W.bits(res.cpu()), "norm": W.bits(nrm.cpu())}
+        stats = PY.check_all(w, got, exp)
+        assert stats["residual_mismatch"] == 0, (k, stats)
+        st = B.ar_fusion_workspace_copy_state(ws)
+        assert st["calls"] == calls0 + k + 1 and st["status"] == 0
+        assert st["lamport_flag"] == (calls0 + k + 1) % 3
+    del g
+    B.ar_fusion_workspace_destroy(ws)
