@@ -43,6 +43,11 @@
  *     aligned (AR_ERR_INVALID otherwise).
  *   - The caller owns every tensor; the library owns the workspace object and,
  *     unless the caller supplied it, the workspace memory.
+ *   - Launching calls may be captured into a CUDA graph once the same call
+ *     (same shapes and options) has run uncaptured, which fills the
+ *     library's host-side launch caches.  The Lamport slot state lives in
+ *     device memory, so every replay reads the slot its own staging filled
+ *     and retires the previous one.
  *   - Device-side waits are bounded: a wait that gives up records
  *     AR_ERR_TIMEOUT in the workspace status word (ar_fusion_workspace_status)
  *     instead of hanging the GPU.
