@@ -3,6 +3,7 @@ header declares, and rejects invalid arguments before any CUDA call."""
 import ctypes
 import os
 import re
+import subprocess
 
 import pytest
 
@@ -125,3 +126,17 @@ def test_binding_fails_loudly_without_library(tmp_path):
             mod.load(str(tmp_path / "nope.so"))
     finally:
         mod._lib = saved
+
+
+def test_plain_c_program_uses_the_library(L, tmp_path):
+    # the header compiles as C99 with a C compiler and the library links and
+    # answers from C (entry points that need no GPU)
+    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "c_abi_check.c")
+    exe = tmp_path / "c_abi_check"
+    libdir = os.path.dirname(B.LIB_PATH)
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", HEADER_DIR, src,
+                        "-o", str(exe), "-L", libdir, "-larfusion", f"-Wl,-rpath,{libdir}"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
