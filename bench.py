@@ -333,7 +333,8 @@ def run_sweep(args):
                           "l2": "inputs just staged (L2-resident)" if lam or byts < 129e6 else "inputs > L2",
                           "status": rc}), flush=True)
 
-    for w in W.FUSED + [W.FP32_DECODE, W.FP32_PREFILL]:
+    for w in W.FUSED + [W.NVFP4_PREFILL.with_(name="r8_t8192_h7168_res_nvfp4_fp16", dtype="fp16"),
+                        W.FP32_DECODE, W.FP32_PREFILL]:
         inp = W.make_fused_inputs(w)
         P, X, G = inp.partials.to(dev), inp.residual.to(dev), inp.gamma.to(dev)
         pat = B.PATTERNS[w.pattern]

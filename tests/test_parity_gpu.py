@@ -245,8 +245,9 @@ def test_lamport_sequence_state_and_retired_slot_clear():
     B.ar_fusion_workspace_destroy(ws)
 
 
-def test_lamport_sentinel_pairs_are_flipped_on_stage():
-    w = W.TINY.with_(seed=5)
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_lamport_sentinel_pairs_are_flipped_on_stage(dtype):
+    w = W.TINY.with_(seed=5, dtype=dtype)
     inp = W.make_fused_inputs(w)
     p16 = inp.partials.view(torch.int16)
     p16[:, :, 0] = 0                       # (lo=+0, hi=-0): the -0.0f sentinel word
