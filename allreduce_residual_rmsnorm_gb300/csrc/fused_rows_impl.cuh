@@ -141,13 +141,16 @@ cudaError_t launch_fused_rows_t(int variant, const FusedArgs& a, const LaunchCfg
             C = 1;
         int vpt = (Hv + C - 1) / C <= one_vec_max ? 1 : pow2_at_least((Hv + 511) / 512);
         // Light 16-bit rows (513..1024 vectors, at most 4 ranks, at most 3072
-        // rank-vectors = 48 KB of partials per row): two rows per SM at two
-        // vectors per thread instead of one 1024-thread row.  Measured (us,
-        // back-to-back / inputs evicted): R=3, H=4104, T=8192: 73.6 / 81.0 vs
-        // 100.3 / 111.5; R=2, H=6144: 86.4 / 90.2 vs 95.1 / 108.2; R=4,
-        // H=6144: 111.2 / 116.8 vs 118.8 / 131.5; heavier rows lose (R=4,
-        // H=8192: 157.5 / 152.5 vs 143.2 / 154.4).
-        if (D::bytes == 2 && C == 1 && rmax <= 4 && Hv > 512 && Hv <= 1024 && a.R * Hv <= 3072)
+        // rank-vectors = 48 KB of partials per row), with at least two rows
+        // per SM: two rows per SM at two vectors per thread instead of one
+        // 1024-thread row (decode sizes keep one vector per thread).
+        // Measured (us, back-to-back / inputs evicted): R=3, H=4104, T=8192:
+        // 73.6 / 81.0 vs 100.3 / 111.5; R=2, H=6144: 86.4 / 90.2 vs
+        // 95.1 / 108.2; R=4, H=6144: 111.2 / 116.8 vs 118.8 / 131.5.  Heavier
+        // rows lose (R=4, H=8192, T=8192: 157.5 / 152.5 vs 143.2 / 154.4; at
+        // T=2048 with FP8 output: 46.6 / 52.4 vs 45.3 / 54.5).
+        if (D::bytes == 2 && C == 1 && rmax <= 4 && Hv > 512 && Hv <= 1024 &&
+            a.R * Hv <= 3072 && a.T >= 2 * c.sms)
             vpt = 2;
         if (vpt > 8)
             return cudaErrorInvalidValue;

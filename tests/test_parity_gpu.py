@@ -87,9 +87,10 @@ EDGE = [
     (8, 33, 2048, "fp16", W.RES_NORM), (6, 17, 7176, "bf16", W.RES_NORM_FP8),
     (2, 3, 32768, "bf16", W.RES_QUANT_NVFP4), (16, 2, 32768, "fp16", W.RES_NORM),
     (8, 200, 4096, "bf16", W.RES_NORM_NVFP4), (1, 500, 7168, "fp16", W.RES_QUANT_FP8),
-    # light rows run two per SM (<= 4 ranks, 513..1024 vectors, R x vectors <= 3072)
-    (3, 37, 6160, "bf16", W.RES_NORM_NVFP4), (4, 50, 4104, "fp16", W.RES_NORM_FP8),
-    (2, 100, 8192, "bf16", W.RES_QUANT_FP8),
+    # two rows per SM (<= 4 ranks, 513..1024 vectors, <= 3072 rank-vectors,
+    # at least 2 rows per SM); the last one stays one row per SM
+    (3, 320, 6160, "bf16", W.RES_NORM_NVFP4), (4, 350, 4104, "fp16", W.RES_NORM_FP8),
+    (2, 400, 8192, "bf16", W.RES_QUANT_FP8), (4, 333, 8192, "bf16", W.RES_NORM),
 ]
 
 
