@@ -621,6 +621,7 @@ def main():
         tps, rows, dt, threads = cpu_oracle_sample(w, inp)
         tps1, rows1, dt1, _ = cpu_oracle_sample(w, inp, target_s=3.0, min_rows=4, threads=1)
         line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                                "gbs": tps * bytes_alg / T / 1e9,
                                 "sample": f"rows 0..{rows} of {w.T} ({dt:.1f} s): fused rows + amax "
                                           "+ NVFP4, C oracle, row-parallel threads",
                                 "value_1thread": tps1,
