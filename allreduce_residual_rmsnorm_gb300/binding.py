@@ -128,6 +128,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.ar_fusion_workspace_set_scale_layout.argtypes = [_vp, _i]
     L.ar_fusion_sum_ex.argtypes = [ctypes.POINTER(_vp), _i, ctypes.c_size_t, _i, _i, _vp, _vp]
     L.ar_fusion_workspace_stage.argtypes = [_vp, _i, _vp, _i, _i, _vp]
+    L.ar_fusion_workspace_partial_ptr.argtypes = [_vp, _i, _i, _i, _vp, ctypes.POINTER(_vp)]
     L.ar_fusion_run.argtypes = [_vp, ctypes.POINTER(_vp), _i, _i, _i, _i, _vp, _vp,
                                 ctypes.c_float, _i, _vp, _vp, _vp, _vp, _vp, _vp]
     L.ar_fusion_norm_amax.argtypes = [_vp, ctypes.POINTER(_vp), _i, _i, _i, _i, _vp, _vp,
@@ -143,7 +144,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                  "ar_fusion_workspace_set_launch", "ar_fusion_workspace_set_accumulate",
                  "ar_fusion_workspace_set_scale_layout",
                  "ar_fusion_sum_ex",
-                 "ar_fusion_workspace_stage", "ar_fusion_run", "ar_fusion_norm_amax",
+                 "ar_fusion_workspace_stage", "ar_fusion_workspace_partial_ptr",
+                 "ar_fusion_run", "ar_fusion_norm_amax",
                  "ar_fusion_sum", "ar_fusion_run_noalloc"):
         getattr(L, name).restype = _i
     _lib = L
@@ -309,6 +311,15 @@ def ar_fusion_workspace_stage(ws: Workspace, rank: int, src: torch.Tensor, token
         tokens = src.shape[0] if src.dim() >= 2 else src.numel() // ws.hidden_dim
     _check(lib().ar_fusion_workspace_stage(ws.handle, rank, _ptr(src), tokens, mode,
                                            _stream(stream)))
+
+
+def ar_fusion_workspace_partial_ptr(ws: Workspace, rank: int, tokens: int,
+                                    mode: int = AR_MODE_AUTO, stream=None) -> int:
+    """Device address where rank `rank`'s [tokens, hidden] partial is staged."""
+    out = ctypes.c_void_p()
+    _check(lib().ar_fusion_workspace_partial_ptr(ws.handle, rank, tokens, mode, _stream(stream),
+                                                 ctypes.byref(out)))
+    return out.value
 
 
 def ar_fusion_run(ws: Workspace, partials, residual_in: torch.Tensor, gamma: torch.Tensor,

@@ -664,6 +664,35 @@ int ar_fusion_workspace_stage(ar_fusion_ws* ws, int rank, const void* src, int t
     return AR_OK;
 }
 
+int ar_fusion_workspace_partial_ptr(ar_fusion_ws* ws, int rank, int tokens, int mode,
+                                    void* stream, void** out)
+{
+    if (!ws || !out)
+        return fail(AR_ERR_INVALID, "workspace or out is NULL");
+    *out = nullptr;
+    if (rank < 0 || rank >= ws->R)
+        return fail(AR_ERR_INVALID, "rank %d outside 0..%d", rank, ws->R - 1);
+    if (mode < AR_MODE_AUTO || mode > AR_MODE_BUFFER)
+        return fail(AR_ERR_INVALID, "mode %d unknown", mode);
+    if (tokens < 1)
+        return fail(AR_ERR_INVALID, "tokens %d < 1", tokens);
+    if (tokens > ws->maxT)
+        return fail(AR_ERR_CAPACITY, "tokens %d > max_token_num %d", tokens, ws->maxT);
+    mode = resolve_mode(ws, mode, tokens);
+    const uint64_t eb = (uint64_t)elem_bytes(ws->dtype);
+    if (mode == AR_MODE_BUFFER) {
+        *out = ws->base + ws->buffer_off + (uint64_t)rank * ws->maxT * ws->H * eb;
+        return AR_OK;
+    }
+    ar_fusion_state st;
+    int rc = ar_fusion_workspace_copy_state(ws, stream, &st);
+    if (rc)
+        return rc;
+    *out = ws->base + ws->lamport_off + (uint64_t)(st.lamport_flag % 3u) * ws->slot_bytes +
+           (uint64_t)rank * tokens * ws->H * eb;
+    return AR_OK;
+}
+
 int ar_fusion_run(ar_fusion_ws* ws, const void* const* partials, int nranks, int tokens,
                   int hidden_dim, int dtype, const void* residual_in, const void* gamma,
                   float eps, int pattern, void* residual_out, void* norm_out, void* quant_out,

@@ -292,6 +292,24 @@ int ar_fusion_workspace_set_scale_layout(ar_fusion_ws* ws, int layout);
 int ar_fusion_workspace_stage(ar_fusion_ws* ws, int rank, const void* src, int tokens, int mode,
                               void* stream);
 
+/* Device address where rank `rank`'s partial of a `tokens`-row call is staged,
+ * for producers that write it in place instead of calling
+ * ar_fusion_workspace_stage (a matmul epilogue, or a peer's push where the
+ * ranks are GPUs).  mode as in ar_fusion_workspace_stage:
+ *   AR_MODE_BUFFER: buffer region + rank * max_token_num * hidden elements;
+ *     host arithmetic, no CUDA call.
+ *   AR_MODE_LAMPORT: current slot + rank * tokens * hidden elements; reads the
+ *     slot index from the device (synchronises `stream`).  The producer must
+ *     write every element of the [tokens][hidden] block and no 32-bit word
+ *     equal to 0x80000000 (write such a -0.0f word as +0.0f, as the staging
+ *     kernel does), ordered before the ar_fusion_run that reads it; the slot
+ *     changes with every Lamport call.
+ * `*out` receives the address (16-byte aligned; 32-byte for fp32).
+ * Errors: AR_ERR_INVALID (NULL, rank, mode, tokens < 1), AR_ERR_CAPACITY
+ * (tokens > max_token_num), AR_ERR_CUDA. */
+int ar_fusion_workspace_partial_ptr(ar_fusion_ws* ws, int rank, int tokens, int mode,
+                                    void* stream, void** out);
+
 /* ---------------------------------------------------------- fused call -- */
 
 /* The fused epilogue (allreduce_fusion_op, TensorRT-LLM allReduceFusionKernels.cu).

@@ -140,3 +140,8 @@ def test_plain_c_program_uses_the_library(L, tmp_path):
     assert r.returncode == 0, r.stderr
     r = subprocess.run([str(exe)], capture_output=True, text=True)
     assert r.returncode == 0, r.stdout + r.stderr
+
+
+def test_partial_ptr_rejects_bad_arguments_before_cuda(L):
+    out = ctypes.c_void_p()
+    assert L.ar_fusion_workspace_partial_ptr(None, 0, 16, 0, None, ctypes.byref(out)) == B.AR_ERR_INVALID

@@ -591,3 +591,44 @@ def test_graph_replay_of_stage_and_run_advances_the_lamport_slots(pdl):
         assert st["lamport_flag"] == (calls0 + k + 1) % 3
     del g
     B.ar_fusion_workspace_destroy(ws)
+
+
+# ------------------------------------------------- partials written in place
+
+@pytest.mark.parametrize("mode", [B.AR_MODE_BUFFER, B.AR_MODE_LAMPORT])
+def test_partials_written_in_place_at_partial_ptr(mode):
+    # a producer writes each rank's block at ar_fusion_workspace_partial_ptr
+    # (no staging kernel); the run then reads it.  In Lamport mode the
+    # address moves with every call and the producer writes no -0.0f word.
+    w = W.DECODE.with_(T=96)
+    ws = make_ws(w, mem=True)
+    B.ar_fusion_workspace_set_mode(ws, mode)
+    info = B.ar_fusion_workspace_info(ws)
+    mem = ws.mem
+    addrs = set()
+    for k in range(4):
+        inp = W.make_fused_inputs(w.with_(seed=700 + k))
+        for r in range(w.R):
+            ptr = B.ar_fusion_workspace_partial_ptr(ws, r, w.T, mode)
+            assert ptr % 16 == 0
+            addrs.add(ptr)
+            words = inp.partials[r].contiguous().view(torch.int32)
+            if mode == B.AR_MODE_LAMPORT:
+                words = torch.where(words == -2 ** 31, torch.zeros_like(words), words)
+            block = words.view(torch.uint8).reshape(-1)
+            off = ptr - info["base"]
+            mem[off:off + block.numel()].copy_(block)
+        X, G = inp.residual.cuda(), inp.gamma.cuda()
+        res, nrm = torch.empty_like(X), torch.empty_like(X)
+        B.ar_fusion_run(ws, None, X, G, w.eps, B.PATTERNS[w.pattern], res, nrm)
+        torch.cuda.synchronize()
+        exp = PY.oracle_expected(w, inp, lamport_flip=mode == B.AR_MODE_LAMPORT)
+        got = {"residual": W.bits(res.cpu()), "norm": W.bits(nrm.cpu())}
+        stats = PY.check_all(w, got, exp)
+        assert stats["residual_mismatch"] == 0, (k, stats)
+        st = B.ar_fusion_workspace_copy_state(ws)
+        assert st["status"] == 0
+        assert st["calls"] == (k + 1 if mode == B.AR_MODE_LAMPORT else 0)
+    # buffer mode: one fixed region per rank; Lamport: the three slots rotate
+    assert len(addrs) == (w.R if mode == B.AR_MODE_BUFFER else 3 * w.R)
+    B.ar_fusion_workspace_destroy(ws)
