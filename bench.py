@@ -517,7 +517,7 @@ def main():
     value, total_ms = aggregate(world, T, args.steps, total_ms, pg, dev)
 
     # ---- end to end: pinned host inputs -> device, run, outputs -> host
-    e2e_steps = 0 if (args.no_e2e or args.profile) else (args.e2e_steps or max(3, min(args.steps, 10)))
+    e2e_steps = 0 if (args.no_e2e or args.profile) else (args.e2e_steps or max(3, min(args.steps, 30)))
     Ph = inp["P"].pin_memory()
     Xh = inp["X"].pin_memory()
     Pd = torch.empty_like(P)
