@@ -24,6 +24,8 @@
 #include "fused_core.cuh"
 
 #include <mutex>
+#include <set>
+#include <utility>
 
 namespace arf {
 
@@ -350,16 +352,22 @@ cudaError_t launch_t(const FusedArgs& a, const LaunchCfg& c)
     if (S < 2)
         return cudaErrorInvalidValue;
     const uint32_t smem = (uint32_t)S * stage_bytes + kSmemTail;
+    // the shared-memory opt-in is a per-device function attribute: set once
+    // per (device, instantiation)
     static std::mutex mu;
-    static bool attr_set[3][9] = {};
+    static std::set<std::pair<int, const void*>> attr_set;
     {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess)
+            return e;
         std::lock_guard<std::mutex> lk(mu);
-        if (!attr_set[D::id][vpt]) {
-            cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)kSmemLimit);
+        if (!attr_set.count({dev, fn})) {
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kSmemLimit);
             if (e != cudaSuccess)
                 return e;
-            attr_set[D::id][vpt] = true;
+            attr_set.insert({dev, fn});
         }
     }
     int grid = c.sms < a.T ? c.sms : a.T;

@@ -7,6 +7,8 @@
 // the n % 8 tail elements done one by one (the page's vectorSum drops nothing
 // either: its 32-bit tail loop covers the rest).  Any misaligned pointer:
 // element-wise kernel.
+#include <atomic>
+
 #include "ar_common.cuh"
 #include "ar_internal.h"
 
@@ -168,13 +170,15 @@ static cudaError_t launch_t(const SumArgs& a, const LaunchCfg& c)
     }
     const int rmax = a.R <= 2 ? 2 : a.R <= 4 ? 4 : a.R <= 8 ? 8 : 16;
     const void* fn = sum_fn<D>(rmax);
-    static int cached[3][17] = {};                 // blocks per SM, per type and RMAX
-    int per_sm = cached[D::id][rmax];
+    // blocks per SM, per type and RMAX (atomic: calls may come from several
+    // host threads; every writer stores the same value)
+    static std::atomic<int> cached[3][17] = {};
+    int per_sm = cached[D::id][rmax].load(std::memory_order_relaxed);
     if (per_sm == 0) {
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, 0) != cudaSuccess ||
             per_sm < 1)
             per_sm = 1;
-        cached[D::id][rmax] = per_sm;
+        cached[D::id][rmax].store(per_sm, std::memory_order_relaxed);
     }
     const uint64_t nvec = a.n / 8;
     // two vectors per thread per step; at least one block (the tail needs it)
