@@ -145,3 +145,29 @@ def test_plain_c_program_uses_the_library(L, tmp_path):
 def test_partial_ptr_rejects_bad_arguments_before_cuda(L):
     out = ctypes.c_void_p()
     assert L.ar_fusion_workspace_partial_ptr(None, 0, 16, 0, None, ctypes.byref(out)) == B.AR_ERR_INVALID
+
+
+def test_last_error_is_per_thread(L):
+    # each host thread reads the message of its own last failure
+    import threading
+    n = ctypes.c_size_t()
+    results = {}
+    barrier = threading.Barrier(4)
+
+    def worker(k):
+        hidden = 480 + k                   # not a multiple of 8: AR_ERR_INVALID naming it
+        barrier.wait()
+        for _ in range(200):
+            rc = L.ar_fusion_workspace_bytes(2, 16, hidden, 0, ctypes.byref(n))
+            msg = L.ar_fusion_last_error().decode()
+            if rc != B.AR_ERR_INVALID or str(hidden) not in msg:
+                results[k] = (rc, msg)
+                return
+        results[k] = "ok"
+
+    ts = [threading.Thread(target=worker, args=(k,)) for k in range(1, 5)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    assert all(v == "ok" for v in results.values()), results
