@@ -98,6 +98,33 @@ constexpr uint32_t kRingTarget = 163840; // bytes of stages per block
 
 }  // namespace
 
+// row_rstd of the consumer warps that also publishes, between the same two
+// barriers, one snapshot of the abort flag taken by a single thread: every
+// consumer warp then takes the same decision to stop after this row.  (A warp
+// reading the flag on its own could leave while the others, having read it
+// before the producer set it, wait for it at the next row's barrier.)
+__device__ __forceinline__ float consumer_row_rstd(DF ss, DF* slots, float* rstd_slot,
+                                                   int* stop_slot, volatile int* abort_flag,
+                                                   int warp, int lane, int nw, int H, float eps,
+                                                   NamedSync sync, bool& stop)
+{
+    ss = df_warp_sum(ss);
+    if (lane == 0)
+        slots[warp] = ss;
+    sync();
+    if (warp == 0) {
+        DF v = lane < nw ? slots[lane] : DF{0.0f, 0.0f};
+        v = df_warp_sum(v);
+        if (lane == 0) {
+            *rstd_slot = inv_rms(v, H, eps);
+            *stop_slot = *abort_flag;
+        }
+    }
+    sync();
+    stop = *reinterpret_cast<volatile int*>(stop_slot) != 0;
+    return *rstd_slot;
+}
+
 // Ring position: stage index and the parity of its current use.
 struct Ring {
     uint32_t s = 0, ph = 0;
@@ -145,6 +172,7 @@ fused_pipe_kernel(const FusedArgs a, const int S, const int NC)
     DF* red = reinterpret_cast<DF*>(empty + kMaxStages);   // [2][32]
     float* rstd_sh = reinterpret_cast<float*>(red + 64);   // [2]
     volatile int* abort_flag = reinterpret_cast<volatile int*>(rstd_sh + 2);
+    int* stop_sh = const_cast<int*>(abort_flag) + 1;       // [2]: per-row snapshots of abort_flag
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
@@ -240,8 +268,10 @@ fused_pipe_kernel(const FusedArgs a, const int S, const int NC)
             float acc[KPS][8];
             V xr[KPS];
             for (int u = 0; ok && u <= R; ++u) {
-                if (!mbar_wait(full0 + 8u * ring.s, ring.ph, tmo)) {
-                    record_error(a.state, AR_ERR_TIMEOUT, -1);
+                // one outcome per warp, so that its lanes stay converged
+                if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8u * ring.s, ring.ph, tmo))) {
+                    if (lane == 0)
+                        record_error(a.state, AR_ERR_TIMEOUT, -1);
                     *abort_flag = 1;
                     ok = false;
                     break;
@@ -284,10 +314,12 @@ fused_pipe_kernel(const FusedArgs a, const int S, const int NC)
                 }
             }
         }
-        const float rstd = row_rstd(ss, red + parity * 32, &rstd_sh[parity], warp, lane, ncw, H,
-                                    a.eps, NamedSync{NC});
+        bool stop = false;
+        const float rstd = consumer_row_rstd(ss, red + parity * 32, &rstd_sh[parity],
+                                             &stop_sh[parity], abort_flag, warp, lane, ncw, H,
+                                             a.eps, NamedSync{NC}, stop);
         parity ^= 1;
-        if (*abort_flag)
+        if (stop)
             break;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
