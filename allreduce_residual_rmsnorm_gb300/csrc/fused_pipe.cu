@@ -342,17 +342,10 @@ const void* pipe_fn(int vpt)
     case 1: return (const void*)fused_pipe_kernel<D, 1>;
     case 2: return (const void*)fused_pipe_kernel<D, 2>;
     case 4: return (const void*)fused_pipe_kernel<D, 4>;
+    case 6: return (const void*)fused_pipe_kernel<D, 6>;
     case 8: return (const void*)fused_pipe_kernel<D, 8>;
     default: return nullptr;
     }
-}
-
-int pow2_at_least(int x)
-{
-    int p = 1;
-    while (p < x)
-        p <<= 1;
-    return p;
 }
 
 template <class D>
@@ -360,8 +353,13 @@ cudaError_t launch_t(const FusedArgs& a, const LaunchCfg& c)
 {
     const int Hv = a.H / 8;
     // at most 512 consumer threads: more consumer warps cost more barrier
-    // arrivals per byte than they win in latency hiding (measured at H = 7168)
-    const int vpt = pow2_at_least((Hv + 511) / 512);
+    // arrivals per byte than they win in latency hiding (measured at H = 7168).
+    // Vectors per thread: ceil(Hv / 512) rounded up to 1, 2, 4, 6 or 8 (even,
+    // for two-slice groups); 6 rather than 8 keeps up to 16 consumer warps for
+    // 2049..3072 vectors (bf16 R = 8, H = 20480: 242.4 vs 284.2 us; R = 4:
+    // 314.0 vs 377.2 us; H = 16392: 273.9 vs 350.2 us).
+    const int q = (Hv + 511) / 512;
+    const int vpt = q <= 2 ? q : (q + 1) / 2 * 2;
     const void* fn = pipe_fn<D>(vpt);
     if (!fn)
         return cudaErrorInvalidValue;

@@ -125,8 +125,9 @@ enum ar_mode {
  * pipe for inputs ((nranks + 1) * tokens * hidden elements) of at least
  * 96 MiB outside Lamport mode when a row needs more than one vector of 8
  * elements per thread of a row block (hidden > 7168 bf16/fp16 with more than
- * 4 ranks, > 8192 with up to 4, > 4096 fp32), or nranks > 8 with rows of
- * more than 8 KB; else one row per thread block. */
+ * 4 ranks, > 8192 with up to 4, > 4096 fp32; with 2 ranks only above 2048
+ * vectors), or nranks > 8 with rows of more than 8 KB; else one row per
+ * thread block. */
 enum ar_variant {
     AR_VARIANT_AUTO = 0,
     AR_VARIANT_WARP_ROW = 1,  /* one row per warp (small hidden) */

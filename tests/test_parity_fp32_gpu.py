@@ -49,7 +49,7 @@ EDGE32 = [
     (16, 7, 520, W.RES_NORM_FP8), (2, 37, 1000, W.RES_QUANT_FP8), (7, 9, 1024, W.RES_NORM_NVFP4),
     (4, 13, 4104, W.RES_NORM), (8, 33, 2048, W.RES_NORM), (6, 17, 7176, W.RES_NORM_FP8),
     (2, 3, 32768, W.RES_QUANT_NVFP4), (16, 2, 32768, W.RES_NORM), (8, 200, 4096, W.RES_NORM_NVFP4),
-    (1, 500, 16384, W.RES_QUANT_FP8),
+    (1, 500, 16384, W.RES_QUANT_FP8), (2, 3, 20480, W.RES_NORM_FP8),
 ]
 
 
@@ -162,6 +162,8 @@ def test_fp32_vector_sum(R, N, offset):
     (8, 256, 7168, "fp32", B.AR_VARIANT_CTA_ROW),       # 66 MB
     (16, 512, 4096, "fp32", B.AR_VARIANT_BULK_PIPE),    # 16 ranks of 16 KB rows
     (4, 2048, 512, "bf16", B.AR_VARIANT_WARP_ROW),
+    (2, 2048, 12288, "bf16", B.AR_VARIANT_CTA_ROW),     # two ranks: row kernel up to 2048 vectors
+    (2, 1024, 20480, "bf16", B.AR_VARIANT_BULK_PIPE),   # beyond that the pipe
 ])
 def test_automatic_variant_choice(R, T, H, dtype, expect):
     w = W.FusedWorkload(f"auto_{R}_{T}_{H}_{dtype}", R=R, T=T, H=H, dtype=dtype,

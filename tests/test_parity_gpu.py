@@ -86,6 +86,7 @@ EDGE = [
     (7, 9, 1024, "bf16", W.RES_NORM_NVFP4), (4, 13, 1032, "bf16", W.RES_NORM),
     (8, 33, 2048, "fp16", W.RES_NORM), (6, 17, 7176, "bf16", W.RES_NORM_FP8),
     (2, 3, 32768, "bf16", W.RES_QUANT_NVFP4), (16, 2, 32768, "fp16", W.RES_NORM),
+    (3, 5, 20480, "bf16", W.RES_NORM_NVFP4), (5, 4, 16392, "fp16", W.RES_NORM),
     (8, 200, 4096, "bf16", W.RES_NORM_NVFP4), (1, 500, 7168, "fp16", W.RES_QUANT_FP8),
     # two rows per SM (<= 4 ranks, 513..1024 vectors, <= 3072 rank-vectors,
     # at least 2 rows per SM); the last one stays one row per SM
