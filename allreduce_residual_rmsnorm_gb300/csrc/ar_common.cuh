@@ -462,18 +462,9 @@ __host__ __device__ __forceinline__ void two_sum(float a, float b, float& s, flo
     err = rn_add(rn_add(a, -rn_add(s, -bb)), rn_add(b, -bb));
 }
 
-__host__ __device__ __forceinline__ void df_add_term(DF& a, float t)
-{
-    float s, err;
-    two_sum(a.hi, t, s, err);
-    a.hi = s;
-    a.lo = rn_add(a.lo, err);
-}
-
-// df_add_term for a non-negative running sum and term (sums of squares):
-// ordering the two by max / min makes Dekker's fast two-sum exact, one
-// operation fewer than TwoSum.  The new high part is still hi + t itself, so
-// a NaN term propagates as before.
+// a += t for a non-negative running sum and term (sums of squares): ordering
+// the two by max / min makes Dekker's fast two-sum exact (one operation fewer
+// than TwoSum); the new high part is hi + t itself, so a NaN term propagates.
 __host__ __device__ __forceinline__ void df_add_nonneg(DF& a, float t)
 {
     const float s = rn_add(a.hi, t);

@@ -1,8 +1,8 @@
 // Host-side check of the double-float sum-of-squares helpers of
 // ar_common.cuh (the same source the kernels use, compiled for the CPU):
-// per-thread accumulation (TwoSum, and the fast two-sum for non-negative
-// terms) followed by a butterfly of df_add, as in a warp reduction, must give
-// the exact sum of squares rounded once to fp32.
+// per-thread accumulation (the fast two-sum for non-negative terms) followed
+// by a butterfly of df_add, as in a warp reduction, must give the exact sum
+// of squares rounded once to fp32, with every lane ending on the same bits.
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -28,7 +28,6 @@ int main()
     std::uniform_int_distribution<int> sign(0, 1);
     int bad = 0, total = 0;
     for (int trial = 0; trial < 800; ++trial) {
-        const bool fast = trial & 1;                         // df_add_nonneg on odd trials
         const int lanes = 32, per = 8 * (1 + (trial / 2) % 32);  // up to 8192 terms per row
         DF acc[32];
         long double exact = 0.0L;
@@ -40,10 +39,7 @@ int main()
                     y = -y;
                 const float t = y * y;                       // exact: 8-bit significand
                 exact += (long double)t;
-                if (fast)
-                    arf::df_add_nonneg(acc[l], t);
-                else
-                    arf::df_add_term(acc[l], t);
+                arf::df_add_nonneg(acc[l], t);
             }
         }
         for (int m = 16; m >= 1; m >>= 1) {                  // xor butterfly
