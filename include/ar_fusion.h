@@ -185,7 +185,7 @@ typedef struct ar_fusion_state {
     uint64_t comm_size;      /* bytes of one Lamport slot */
     uint64_t clear_size;     /* elements of the retired slot still to be cleared */
     int32_t status;          /* AR_OK or the first device-side error (AR_ERR_TIMEOUT) */
-    int32_t detail;          /* where it happened: row * 32 + rank, or -1 */
+    int32_t detail;          /* where it happened (see ar_fusion_workspace_status), or -1 */
     uint64_t calls;          /* Lamport-mode calls since create / reset */
 } ar_fusion_state;
 
@@ -228,7 +228,10 @@ int ar_fusion_workspace_copy_state(ar_fusion_ws* ws, void* stream, ar_fusion_sta
 
 /* Synchronise `stream`, read the device status word: returns AR_OK, the
  * recorded device error (AR_ERR_TIMEOUT), or AR_ERR_CUDA.  *detail (may be
- * NULL) receives row * 32 + rank of the first failed wait, or -1. */
+ * NULL) receives where the first wait gave up: row * 32 + rank for a Lamport
+ * poll; for the bulk-copy pipe -1 (a stage wait of the consumers), -2 (the
+ * producer waiting for a free stage) or -3 (its final wait for copies in
+ * flight); -1 when nothing failed. */
 int ar_fusion_workspace_status(ar_fusion_ws* ws, void* stream, int* detail);
 
 /* Re-initialise on `stream`: Lamport region back to -0.0f words, slot index
