@@ -633,3 +633,45 @@ def test_partials_written_in_place_at_partial_ptr(mode):
     # buffer mode: one fixed region per rank; Lamport: the three slots rotate
     assert len(addrs) == (w.R if mode == B.AR_MODE_BUFFER else 3 * w.R)
     B.ar_fusion_workspace_destroy(ws)
+
+
+def test_long_mixed_sequence_keeps_the_lamport_invariants():
+    # 60 calls on one workspace: Lamport calls of varying token counts mixed
+    # with staged buffer-mode calls and caller-partial calls.  After every
+    # Lamport call the slot the next Lamport call will read must hold only
+    # sentinel words (its retired data was cleared two calls ago), and the
+    # slot counter must count exactly the Lamport calls.
+    import random
+    w = W.FusedWorkload("mixed", R=4, T=128, H=1024, pattern=W.RES_NORM)
+    ws = make_ws(w, mem=True)
+    info = B.ar_fusion_workspace_info(ws)
+    slot_b = info["lamport_comm_bytes"]
+    lam_off = info["lamport"] - info["base"]
+    sent = torch.tensor(-2 ** 31, dtype=torch.int32, device="cuda")
+    rng = random.Random(3)
+    lamport_calls = 0
+    for k in range(60):
+        kind = rng.choice(["lamport", "lamport", "buffer", "caller"])
+        T = rng.choice([1, 5, 64, 100, 128])
+        wk = w.with_(T=T, seed=900 + k)
+        inp = W.make_fused_inputs(wk)
+        if kind == "caller":
+            got = PY.run_gpu(ws, wk, inp, staged=False)
+            exp = PY.oracle_expected(wk, inp)
+        else:
+            mode = B.AR_MODE_LAMPORT if kind == "lamport" else B.AR_MODE_BUFFER
+            B.ar_fusion_workspace_set_mode(ws, mode)
+            got = PY.run_gpu(ws, wk, inp, staged=True)
+            B.ar_fusion_workspace_set_mode(ws, B.AR_MODE_AUTO)
+            exp = PY.oracle_expected(wk, inp, lamport_flip=kind == "lamport")
+        stats = PY.check_all(wk, got, exp)
+        assert stats["residual_mismatch"] == 0, (k, kind, T, stats)
+        st = B.ar_fusion_workspace_copy_state(ws)
+        assert st["status"] == 0, (k, st)
+        if kind == "lamport":
+            lamport_calls += 1
+            nxt = st["lamport_flag"] % 3
+            region = ws.mem[lam_off + nxt * slot_b: lam_off + (nxt + 1) * slot_b].view(torch.int32)
+            assert bool((region == sent).all()), (k, "next slot not fully cleared")
+        assert st["calls"] == lamport_calls and st["lamport_flag"] == lamport_calls % 3
+    B.ar_fusion_workspace_destroy(ws)
