@@ -348,10 +348,14 @@ int pick_variant(const ar_fusion_ws* ws, const FusedArgs& a)
     const int Hv = a.H / 8;
     const uint64_t eb = (uint64_t)elem_bytes(ws->dtype);
     const uint64_t in_bytes = (uint64_t)(a.R + 1) * a.T * a.H * eb;
-    // with two ranks the row kernel holds up to 4 vectors per thread as well
-    // (bf16 R = 2, H = 10240: 312.6 vs 335.5 us; H = 12288: 325.3 vs 352.1 us;
-    // H = 16384: 394.5 vs 394.6 us; H = 20480: 1071.7 vs 468.1 us)
-    const bool wide = Hv > one_vec_threads_for((int)eb, a.R) && !(a.R <= 2 && Hv <= 2048);
+    // The row kernel also keeps 16-bit rows of up to 1536 vectors with at most
+    // 4 ranks (three vectors per thread: R = 4, H = 10240, T = 13104: 276.4 vs
+    // 353.9 us; R = 3, H = 12288: 352.5 vs 409.7 us) and, with two ranks, up
+    // to 2048 vectors (R = 2, H = 16384: 394.5 vs 394.6 us; H = 20480:
+    // 1071.7 vs 468.1 us).  fp32 rows beyond one vector per thread take the
+    // pipe at any rank count (R = 2, H = 12288: 453.5 vs 530.6 us).
+    const bool row_holds = eb == 2 && ((a.R <= 4 && Hv <= 1536) || (a.R <= 2 && Hv <= 2048));
+    const bool wide = Hv > one_vec_threads_for((int)eb, a.R) && !row_holds;
     const bool many_ranks = a.R > 8 && (uint64_t)a.H * eb > 8192;
     if (!a.lamport && !a.amax_out && in_bytes >= (96ull << 20) && (wide || many_ranks) &&
         fused_pipe_supported(ws->dtype, a.H, a.R))

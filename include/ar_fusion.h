@@ -124,10 +124,9 @@ enum ar_mode {
 /* Kernel variant.  AUTO: one row per warp for hidden <= 512; the bulk-copy
  * pipe for inputs ((nranks + 1) * tokens * hidden elements) of at least
  * 96 MiB outside Lamport mode when a row needs more than one vector of 8
- * elements per thread of a row block (hidden > 7168 bf16/fp16 with more than
- * 4 ranks, > 8192 with up to 4, > 4096 fp32; with 2 ranks only above 2048
- * vectors), or nranks > 8 with rows of more than 8 KB; else one row per
- * thread block. */
+ * elements per thread of a row block (bf16/fp16: hidden > 7168 with more
+ * than 4 ranks, > 12288 with 3 or 4, > 16384 with 1 or 2; fp32: > 4096), or
+ * nranks > 8 with rows of more than 8 KB; else one row per thread block. */
 enum ar_variant {
     AR_VARIANT_AUTO = 0,
     AR_VARIANT_WARP_ROW = 1,  /* one row per warp (small hidden) */

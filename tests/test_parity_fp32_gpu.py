@@ -164,6 +164,9 @@ def test_fp32_vector_sum(R, N, offset):
     (4, 2048, 512, "bf16", B.AR_VARIANT_WARP_ROW),
     (2, 2048, 12288, "bf16", B.AR_VARIANT_CTA_ROW),     # two ranks: row kernel up to 2048 vectors
     (2, 1024, 20480, "bf16", B.AR_VARIANT_BULK_PIPE),   # beyond that the pipe
+    (4, 1024, 12288, "bf16", B.AR_VARIANT_CTA_ROW),     # <= 4 ranks: row kernel up to 1536 vectors
+    (4, 1024, 16384, "bf16", B.AR_VARIANT_BULK_PIPE),
+    (2, 1024, 12288, "fp32", B.AR_VARIANT_BULK_PIPE),   # fp32: the pipe beyond 512 vectors
 ])
 def test_automatic_variant_choice(R, T, H, dtype, expect):
     w = W.FusedWorkload(f"auto_{R}_{T}_{H}_{dtype}", R=R, T=T, H=H, dtype=dtype,

@@ -87,6 +87,9 @@ EDGE = [
     (8, 33, 2048, "fp16", W.RES_NORM), (6, 17, 7176, "bf16", W.RES_NORM_FP8),
     (2, 3, 32768, "bf16", W.RES_QUANT_NVFP4), (16, 2, 32768, "fp16", W.RES_NORM),
     (3, 5, 20480, "bf16", W.RES_NORM_NVFP4), (5, 4, 16392, "fp16", W.RES_NORM),
+    # three vectors per thread (<= 4 ranks, 1025..1536 vectors)
+    (3, 7, 10240, "bf16", W.RES_NORM_NVFP4), (4, 33, 12288, "fp16", W.RES_NORM_FP8),
+    (2, 9, 8200, "bf16", W.RES_NORM),
     (8, 200, 4096, "bf16", W.RES_NORM_NVFP4), (1, 500, 7168, "fp16", W.RES_QUANT_FP8),
     # two rows per SM (<= 4 ranks, 513..1024 vectors, <= 3072 rank-vectors,
     # at least 2 rows per SM); the last one stays one row per SM
