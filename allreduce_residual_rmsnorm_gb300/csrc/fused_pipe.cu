@@ -143,12 +143,13 @@ struct Ring {
 // partials of group j, then its residual, then group j + 1.  A consumer
 // therefore finishes the rank sum of KPS vectors before the next group
 // arrives and keeps only the packed y of the row in registers; and a stage is
-// at most KPS * NC vectors (16 KB of bf16 at NC = 512) whatever the hidden
-// size, so the ring holds ~10 copies in flight even for 32768-wide rows.
+// at most KPS * NC vectors (KPS = 2, or 3 for three vectors per thread: at
+// most 24 KB of bf16 at NC = 512) whatever the hidden size, so the ring holds
+// 6 to 10 copies in flight even for 32768-wide rows.
 template <int VPT>
 __host__ __device__ constexpr int pipe_kps()
 {
-    return VPT < 2 ? VPT : 2;
+    return VPT == 3 ? 3 : (VPT < 2 ? VPT : 2);
 }
 
 template <class D, int VPT>
@@ -342,6 +343,7 @@ const void* pipe_fn(int vpt)
     case 1: return (const void*)fused_pipe_kernel<D, 1>;
     case 2: return (const void*)fused_pipe_kernel<D, 2>;
     case 4: return (const void*)fused_pipe_kernel<D, 4>;
+    case 3: return (const void*)fused_pipe_kernel<D, 3>;
     case 6: return (const void*)fused_pipe_kernel<D, 6>;
     case 8: return (const void*)fused_pipe_kernel<D, 8>;
     default: return nullptr;
@@ -354,17 +356,18 @@ cudaError_t launch_t(const FusedArgs& a, const LaunchCfg& c)
     const int Hv = a.H / 8;
     // at most 512 consumer threads: more consumer warps cost more barrier
     // arrivals per byte than they win in latency hiding (measured at H = 7168).
-    // Vectors per thread: ceil(Hv / 512) rounded up to 1, 2, 4, 6 or 8 (even,
-    // for two-slice groups); 6 rather than 8 keeps up to 16 consumer warps for
-    // 2049..3072 vectors (bf16 R = 8, H = 20480: 242.4 vs 284.2 us; R = 4:
-    // 314.0 vs 377.2 us; H = 16392: 273.9 vs 350.2 us).
+    // Vectors per thread: ceil(Hv / 512), rounded up to an even count above 3
+    // (two-slice groups); 3 (one three-slice group per source row) and 6
+    // rather than 4 and 8 keep up to 16 consumer warps (bf16 R = 8,
+    // H = 10240: 220.5 vs 258.0 us; H = 12288: 218.1 vs 229.9 us; H = 20480:
+    // 242.4 vs 284.2 us; R = 4, H = 20480: 314.0 vs 377.2 us).
     const int q = (Hv + 511) / 512;
-    const int vpt = q <= 2 ? q : (q + 1) / 2 * 2;
+    const int vpt = q <= 3 ? q : (q + 1) / 2 * 2;
     const void* fn = pipe_fn<D>(vpt);
     if (!fn)
         return cudaErrorInvalidValue;
     const int NC = ((Hv + vpt - 1) / vpt + 31) / 32 * 32;
-    const int kps = vpt < 2 ? vpt : 2;
+    const int kps = vpt == 3 ? 3 : (vpt < 2 ? vpt : 2);
     // every slice group must hold at least one vector of the row
     if (NC * (vpt - kps) >= Hv)
         return cudaErrorInvalidValue;
