@@ -343,7 +343,12 @@ const void* pipe_fn(int vpt)
     case 1: return (const void*)fused_pipe_kernel<D, 1>;
     case 2: return (const void*)fused_pipe_kernel<D, 2>;
     case 4: return (const void*)fused_pipe_kernel<D, 4>;
-    case 3: return (const void*)fused_pipe_kernel<D, 3>;
+    case 3:
+        // 16-bit only: a three-slice fp32 group would be 48 KB (a 3-stage ring)
+        if constexpr (D::bytes == 2)
+            return (const void*)fused_pipe_kernel<D, 3>;
+        else
+            return nullptr;
     case 6: return (const void*)fused_pipe_kernel<D, 6>;
     case 8: return (const void*)fused_pipe_kernel<D, 8>;
     default: return nullptr;
@@ -362,7 +367,7 @@ cudaError_t launch_t(const FusedArgs& a, const LaunchCfg& c)
     // H = 10240: 220.5 vs 258.0 us; H = 12288: 218.1 vs 229.9 us; H = 20480:
     // 242.4 vs 284.2 us; R = 4, H = 20480: 314.0 vs 377.2 us).
     const int q = (Hv + 511) / 512;
-    const int vpt = q <= 3 ? q : (q + 1) / 2 * 2;
+    const int vpt = (q <= 3 && (q < 3 || D::bytes == 2)) ? q : (q + 1) / 2 * 2;
     const void* fn = pipe_fn<D>(vpt);
     if (!fn)
         return cudaErrorInvalidValue;

@@ -49,7 +49,7 @@ EDGE32 = [
     (16, 7, 520, W.RES_NORM_FP8), (2, 37, 1000, W.RES_QUANT_FP8), (7, 9, 1024, W.RES_NORM_NVFP4),
     (4, 13, 4104, W.RES_NORM), (8, 33, 2048, W.RES_NORM), (6, 17, 7176, W.RES_NORM_FP8),
     (2, 3, 32768, W.RES_QUANT_NVFP4), (16, 2, 32768, W.RES_NORM), (8, 200, 4096, W.RES_NORM_NVFP4),
-    (1, 500, 16384, W.RES_QUANT_FP8), (2, 3, 20480, W.RES_NORM_FP8),
+    (1, 500, 16384, W.RES_QUANT_FP8), (2, 3, 20480, W.RES_NORM_FP8), (3, 9, 10240, W.RES_NORM_NVFP4),
 ]
 
 
