@@ -429,6 +429,26 @@ def test_nvfp4_encoder_many_values():
 
 # -------------------------------------------------------------- calibration
 
+def test_norm_amax_from_staged_buffer_partials():
+    # partials == NULL: the calibration pass reads the buffer region (never the
+    # Lamport slots, whose state it must leave alone)
+    w = W.FP8_PREFILL.with_(T=200, seed=4)
+    inp = W.make_fused_inputs(w)
+    exp = PY.oracle_expected(w, inp)
+    ws = make_ws(w)
+    P = inp.partials.cuda()
+    for r in range(w.R):
+        B.ar_fusion_workspace_stage(ws, r, P[r], mode=B.AR_MODE_BUFFER)
+    before = B.ar_fusion_workspace_copy_state(ws)
+    amax = torch.full((1,), -1.0, device="cuda")
+    B.ar_fusion_norm_amax(ws, None, inp.residual.cuda(), inp.gamma.cuda(), w.eps, amax)
+    torch.cuda.synchronize()
+    assert float(amax.item()) == exp["amax"]
+    after = B.ar_fusion_workspace_copy_state(ws)
+    assert after["calls"] == before["calls"] and after["lamport_flag"] == before["lamport_flag"]
+    B.ar_fusion_workspace_destroy(ws)
+
+
 def test_norm_amax_matches_oracle():
     for w in (W.FP8_PREFILL.with_(T=256), W.TINY):
         inp = W.make_fused_inputs(w)
