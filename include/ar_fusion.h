@@ -95,7 +95,8 @@ enum ar_status {
     AR_ERR_UNSUPPORTED = -2,  /* valid request outside what the kernels implement */
     AR_ERR_CUDA = -3,         /* a CUDA runtime call failed; see ar_fusion_last_error */
     AR_ERR_TIMEOUT = -4,      /* a bounded device-side wait gave up */
-    AR_ERR_CAPACITY = -5      /* tokens > max_token_num of the workspace */
+    AR_ERR_CAPACITY = -5      /* staged tokens > max_token_num of the workspace
+                                 (or beyond the no-allocation scratch) */
 };
 
 /* Accumulation of the rank sum (TensorRT-LLM allReduceFusionKernels.cu:
@@ -199,7 +200,9 @@ int ar_fusion_workspace_bytes(int tp_size, int max_token_num, int hidden_dim, in
 /* Create a workspace (Workspace constructor of TensorRT-LLM
  * allReduceFusionKernels.cu; FlashInfer trtllm_create_ipc_workspace_for_all_reduce_fusion).
  *   tp_size        R, 1..AR_MAX_RANKS
- *   max_token_num  largest `tokens` any later call may pass, >= 1
+ *   max_token_num  largest `tokens` of a call that reads staged partials
+ *                  (it sizes the buffer region and the Lamport slots), >= 1;
+ *                  calls with caller partials may pass more tokens
  *   hidden_dim     row length, multiple of 8, <= AR_MAX_HIDDEN
  *   dtype          enum ar_dtype
  *   device_mem     NULL: the library allocates (cudaMalloc) and frees the memory.

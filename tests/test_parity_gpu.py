@@ -698,3 +698,20 @@ def test_long_mixed_sequence_keeps_the_lamport_invariants():
             assert bool((region == sent).all()), (k, "next slot not fully cleared")
         assert st["calls"] == lamport_calls and st["lamport_flag"] == lamport_calls % 3
     B.ar_fusion_workspace_destroy(ws)
+
+
+def test_caller_partials_may_exceed_max_token_num():
+    # max_token_num sizes the staging regions only: a call with caller
+    # partials may pass more tokens; a staged one may not
+    w = W.FusedWorkload("beyond_max", R=3, T=300, H=1024, pattern=W.RES_NORM, seed=11)
+    inp = W.make_fused_inputs(w)
+    ws = make_ws(w, max_tokens=64)
+    got = PY.run_gpu(ws, w, inp, staged=False)
+    stats = PY.check_all(w, got, PY.oracle_expected(w, inp))
+    assert stats["residual_mismatch"] == 0
+    X = inp.residual.cuda()
+    with pytest.raises(B.ArFusionError) as e:
+        B.ar_fusion_run(ws, None, X, inp.gamma.cuda(), w.eps, B.PATTERNS[w.pattern],
+                        torch.empty_like(X), torch.empty_like(X))
+    assert e.value.code == B.AR_ERR_CAPACITY
+    B.ar_fusion_workspace_destroy(ws)
