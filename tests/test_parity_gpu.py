@@ -715,3 +715,36 @@ def test_caller_partials_may_exceed_max_token_num():
                         torch.empty_like(X), torch.empty_like(X))
     assert e.value.code == B.AR_ERR_CAPACITY
     B.ar_fusion_workspace_destroy(ws)
+
+
+def test_two_workspaces_on_two_streams_run_independently():
+    # each workspace owns its slots and state: Lamport calls on two streams,
+    # issued alternately without ordering between the streams, stay correct
+    ws_list, streams, cases = [], [], []
+    for k, w in enumerate((W.DECODE.with_(T=96, seed=41), W.TINY.with_(seed=42, T=12))):
+        ws_list.append(make_ws(w))
+        streams.append(torch.cuda.Stream())
+        cases.append(w)
+    outs = []
+    for step in range(6):
+        for k, (ws, s, w) in enumerate(zip(ws_list, streams, cases)):
+            wk = w.with_(seed=w.seed + 100 * step)
+            inp = W.make_fused_inputs(wk)
+            with torch.cuda.stream(s):
+                P = inp.partials.cuda(non_blocking=False)
+                X, G = inp.residual.cuda(), inp.gamma.cuda()
+                res, nrm = torch.empty_like(X), torch.empty_like(X)
+                for r in range(wk.R):
+                    B.ar_fusion_workspace_stage(ws, r, P[r], stream=s)
+                B.ar_fusion_run(ws, None, X, G, wk.eps, B.PATTERNS[wk.pattern], res, nrm, stream=s)
+            outs.append((k, wk, inp, res, nrm, P, X, G))
+    torch.cuda.synchronize()
+    for k, wk, inp, res, nrm, *_ in outs:
+        exp = PY.oracle_expected(wk, inp, lamport_flip=True)
+        got = {"residual": W.bits(res.cpu()), "norm": W.bits(nrm.cpu())}
+        stats = PY.check_all(wk, got, exp)
+        assert stats["residual_mismatch"] == 0, (k, stats)
+    for ws, s in zip(ws_list, streams):
+        st = B.ar_fusion_workspace_copy_state(ws, stream=s)
+        assert st["calls"] == 6 and st["status"] == 0
+        B.ar_fusion_workspace_destroy(ws)
