@@ -376,6 +376,28 @@ def run_sweep(args):
                 # staging stands for the peers' pushes: time stage + call, minus stage
                 us = graph_us(lambda: (stage(), call())) - graph_us(stage)
             report(w, pat, ws, lam, us, cl, pdl)
+        if w is W.NVFP4_PREFILL:
+            # the precision and layout options on the benchmarked workload:
+            # element-type accumulation, NVFP4 scales in the 128 x 4 tile layout
+            B.ar_fusion_workspace_set_launch(ws, 0, 0)
+            sf_swz = torch.zeros(B.swizzled_scale_bytes(w.T, w.H), dtype=torch.uint8, device=dev)
+            for opt in ("acc_element", "sf_swizzled"):
+                B.ar_fusion_workspace_set_accumulate(
+                    ws, B.AR_ACC_ELEMENT if opt == "acc_element" else B.AR_ACC_FP32)
+                B.ar_fusion_workspace_set_scale_layout(
+                    ws, B.AR_SF_SWIZZLED if opt == "sf_swizzled" else B.AR_SF_LINEAR)
+                sfo = sf_swz if opt == "sf_swizzled" else sf
+                stage()
+                us = graph_us(lambda: B.ar_fusion_run(ws, None, X, G, w.eps, pat, out["res"],
+                                                      out["norm"], q, sfo, sc))
+                byts = fused_bytes(w, pat)
+                print(json.dumps({"sweep": w.name, "option": opt, "us": us,
+                                  "gbs": byts / (us * 1e-6) / 1e9,
+                                  "frac_of_copy_peak": byts / (us * 1e-6) / 1e9 / peak}),
+                      flush=True)
+            B.ar_fusion_workspace_set_accumulate(ws, B.AR_ACC_FP32)
+            B.ar_fusion_workspace_set_scale_layout(ws, B.AR_SF_LINEAR)
+            del sf_swz
         eb = 4 if w.dtype == "fp32" else 2
         if (w.R + 3) * w.T * w.H * eb < 2 * l2_bytes:
             # caller partials (no staging), inputs evicted before every call
