@@ -192,13 +192,45 @@ __device__ __forceinline__ uint4 add_packed<Fp16>(const uint4& a, const uint4& b
     return r;
 }
 
-// s[i] = f(rnd(s[i])): the element-type accumulation rounds every partial sum
-// (nothing to do for fp32 elements)
+// Element-type accumulation (every partial sum rounded to the element type).
+// For 16-bit elements the running sum stays packed: its four words ride, as
+// bit copies, in the first four slots of the fp32 array, each rank is one
+// packed add per pair (equal to the fp32 add rounded to the element type, as
+// above), and elem_finish8 unpacks the final sum.  For fp32 elements it is the
+// fp32 sum.
 template <class D>
-__device__ __forceinline__ void round8(float (&s)[8])
+__device__ __forceinline__ void elem_start8(float (&s)[8], const typename D::Vec& v)
 {
-    if constexpr (D::bytes != 4)
-        unpack8<D>(pack8<D>(s), s);
+    if constexpr (D::bytes == 4) {
+        unpack8<D>(v, s);
+    } else {
+        s[0] = __uint_as_float(v.x); s[1] = __uint_as_float(v.y);
+        s[2] = __uint_as_float(v.z); s[3] = __uint_as_float(v.w);
+    }
+}
+
+template <class D>
+__device__ __forceinline__ void elem_add8(float (&s)[8], const typename D::Vec& v)
+{
+    if constexpr (D::bytes == 4) {
+        add8<D>(s, v);
+    } else {
+        const uint4 w = add_packed<D>(make_uint4(__float_as_uint(s[0]), __float_as_uint(s[1]),
+                                                 __float_as_uint(s[2]), __float_as_uint(s[3])),
+                                      v);
+        s[0] = __uint_as_float(w.x); s[1] = __uint_as_float(w.y);
+        s[2] = __uint_as_float(w.z); s[3] = __uint_as_float(w.w);
+    }
+}
+
+template <class D>
+__device__ __forceinline__ void elem_finish8(float (&s)[8])
+{
+    if constexpr (D::bytes != 4) {
+        const uint4 w = make_uint4(__float_as_uint(s[0]), __float_as_uint(s[1]),
+                                   __float_as_uint(s[2]), __float_as_uint(s[3]));
+        unpack8<D>(w, s);
+    }
 }
 
 // Squares of a packed pair, exact (8- or 11-bit significands): fma with a

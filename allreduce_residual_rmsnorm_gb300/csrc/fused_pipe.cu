@@ -291,15 +291,19 @@ fused_pipe_kernel(const FusedArgs a, const int S, const int NC)
                 ring.next((uint32_t)S);
 #pragma unroll
                 for (int kk = 0; kk < KPS; ++kk) {
-                    if (u == 0)
-                        unpack8<D>(w[kk], acc[kk]);
-                    else if (u < R) {
-                        add8<D>(acc[kk], w[kk]);
+                    if (u == 0) {
                         if (a.acc)
-                            round8<D>(acc[kk]);
-                    }
-                    else
+                            elem_start8<D>(acc[kk], w[kk]);
+                        else
+                            unpack8<D>(w[kk], acc[kk]);
+                    } else if (u < R) {
+                        if (a.acc)
+                            elem_add8<D>(acc[kk], w[kk]);
+                        else
+                            add8<D>(acc[kk], w[kk]);
+                    } else {
                         xr[kk] = w[kk];
+                    }
                 }
             }
 #pragma unroll
@@ -307,6 +311,8 @@ fused_pipe_kernel(const FusedArgs a, const int S, const int NC)
                 const int k = j * KPS + kk;
                 const int v = g + k * NC;
                 if (ok && v < Hv) {
+                    if (a.acc)
+                        elem_finish8<D>(acc[kk]);
                     yv[k] = residual_vec<D>(acc[kk], xr[kk], ss);
                     if (pat & AR_RESIDUAL_OUT)
                         st_vec(a.residual_out + roff + (size_t)v * VB, yv[k]);

@@ -68,11 +68,15 @@ __device__ __forceinline__ void fold_ranks(float (&s)[KCH][8],
             for (int rr = 0; rr < RB; ++rr) {
                 if (r0 + rr < R) {
                     if (r0 + rr == 0) {
-                        unpack8<D>(raw[kk][rr], s[kk]);
-                    } else {
-                        add8<D>(s[kk], raw[kk][rr]);
                         if (ELEM)
-                            round8<D>(s[kk]);
+                            elem_start8<D>(s[kk], raw[kk][rr]);
+                        else
+                            unpack8<D>(raw[kk][rr], s[kk]);
+                    } else {
+                        if (ELEM)
+                            elem_add8<D>(s[kk], raw[kk][rr]);
+                        else
+                            add8<D>(s[kk], raw[kk][rr]);
                     }
                 }
             }
@@ -265,6 +269,8 @@ fused_rows_kernel(const FusedArgs a)
                 const int k = k0 + kk;
                 const int v = g + k * G;
                 if (v < Hv) {
+                    if (a.acc)
+                        elem_finish8<D>(s[kk]);
                     const V y = residual_vec<D>(s[kk], xr[kk], ss);
                     yv[k] = y;
                     if (pat & AR_RESIDUAL_OUT)

@@ -63,6 +63,17 @@ template <class D, int RMAX>
 __device__ __forceinline__ typename D::Vec sum_vec(const SumArgs& a,
                                                    const typename D::Vec (&raw)[RMAX])
 {
+    if constexpr (D::bytes == 2) {
+        // element-type adds: one packed add per pair and rank
+        if (a.acc) {
+            typename D::Vec s = raw[0];
+#pragma unroll
+            for (int r = 1; r < RMAX; ++r)
+                if (r < a.R)
+                    s = add_packed<D>(s, raw[r]);
+            return s;
+        }
+    }
     float s[8];
     unpack8<D>(raw[0], s);
 #pragma unroll
@@ -73,8 +84,6 @@ __device__ __forceinline__ typename D::Vec sum_vec(const SumArgs& a,
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 s[i] = __fadd_rn(s[i], t[i]);
-            if (a.acc)
-                round8<D>(s);
         }
     }
     return pack8<D>(s);

@@ -166,6 +166,31 @@ def test_vector_sum_element_type_accumulation():
     assert np.array_equal(oracle.vector_sum(FP16, bits(x), threads=2, acc=1), bits(a))
 
 
+@pytest.mark.parametrize("dtype", [BF16, FP16])
+def test_vector_sum_element_type_special_values_are_chained_library_adds(dtype):
+    # signed zeros, subnormals, ties, the largest finite values, infinities and
+    # NaN: the per-add rounding (with overflow to infinity, -0 + -0 = -0 and
+    # +0 + -0 = +0) follows torch's chained 16-bit adds; NaN only in position
+    tdt = torch.bfloat16 if dtype == BF16 else torch.float16
+    fin = torch.finfo(tdt)
+    pool = torch.tensor([0.0, -0.0, fin.smallest_normal, fin.smallest_normal / 4, -fin.tiny / 8,
+                         1.0, 1.0 + fin.eps, fin.eps / 2, -fin.eps / 2, fin.max, -fin.max,
+                         fin.max / 2, float("inf"), float("-inf"), float("nan"), 0.75],
+                        dtype=torch.float32).to(tdt)
+    g = torch.Generator().manual_seed(5)
+    R, N = 5, 6000
+    x = pool[torch.randint(0, len(pool), (R, N), generator=g)]
+    a = x[0].clone()
+    for r in range(1, R):
+        a = a + x[r]
+    got = oracle.vector_sum(dtype, bits(x), threads=2, acc=1)
+    nan = torch.isnan(a).numpy()
+    assert nan.any() and torch.isinf(a).any()
+    got_t = torch.from_numpy(got.view(np.int16)).view(tdt)
+    assert np.array_equal(torch.isnan(got_t).numpy(), nan)
+    assert np.array_equal(got[~nan], bits(a)[~nan])
+
+
 # ----------------------------------------------------- RMSNorm (steps 3-5)
 
 @pytest.mark.parametrize("H,c", [(8, 1.0), (512, -0.25), (7168, 4.0), (4096, -2.0 ** -6)])

@@ -189,6 +189,61 @@ def test_vector_sum_element_type_accumulation(R, N, dtype, offset):
     assert np.array_equal(W.bits(out.cpu()), exp)
 
 
+# Values that stress the per-add rounding of the element-type sum: signed
+# zeros, subnormals, neighbours one unit in the last place apart, exact halves
+# of a unit (ties), the largest finite values and infinities.
+SPECIALS = {
+    "fp16": [0.0, -0.0, 2.0**-24, -2.0**-24, 3 * 2.0**-24, 2.0**-14, 1.0, 1 + 2.0**-10, 2.0**-11,
+             -2.0**-11, 3 * 2.0**-12, 65504.0, -65504.0, 32768.0, float("inf"), float("-inf")],
+    "bf16": [0.0, -0.0, 2.0**-133, -2.0**-133, 2.0**-126, 1.0, 1 + 2.0**-7, 2.0**-8, -2.0**-8,
+             3 * 2.0**-10, 2.0**127 * 1.9921875, -2.0**127 * 1.9921875, 2.0**127, float("inf"),
+             float("-inf")],
+}
+
+
+def special_draw(dtype, shape, seed, finite=False):
+    pool = [v for v in SPECIALS[dtype] if not finite or abs(v) < 1e4]
+    if not finite:
+        pool.append(float("nan"))
+    vals = torch.tensor(pool, dtype=W.torch_dtype(dtype))
+    rng = np.random.default_rng(seed)
+    x = vals[torch.from_numpy(rng.integers(0, len(pool), size=shape))]
+    # a third of the elements ordinary values, so special and plain terms meet
+    plain = torch.from_numpy(rng.uniform(-2, 2, size=shape)).to(x.dtype)
+    return torch.where(torch.from_numpy(rng.random(shape) < 1 / 3), plain, x)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("R", [2, 5, 8])
+def test_vector_sum_special_values(dtype, R):
+    x = special_draw(dtype, (R, 40_003), seed=R)
+    xd = x.cuda()
+    for acc, oacc in ((B.AR_ACC_ELEMENT, 1), (B.AR_ACC_FP32, 0)):
+        exp = oracle.vector_sum(PY.ODT[dtype], W.bits(x), acc=oacc)
+        out = torch.empty(x.shape[1], dtype=x.dtype, device="cuda")
+        B.ar_fusion_sum_ex([xd[r] for r in range(R)], out, acc)
+        torch.cuda.synchronize()
+        got = out.cpu()
+        nan_e = torch.isnan(W.from_bits(exp, dtype)).numpy()
+        assert np.array_equal(torch.isnan(got).numpy(), nan_e), (acc, "NaN positions")
+        assert np.array_equal(W.bits(got)[~nan_e], exp[~nan_e]), acc
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("variant", [B.AR_VARIANT_WARP_ROW, B.AR_VARIANT_CTA_ROW,
+                                     B.AR_VARIANT_BULK_PIPE])
+def test_element_type_accumulation_special_partials(dtype, variant):
+    # finite specials only: the row's norm stays finite
+    w = W.FusedWorkload(f"acc_special_{dtype}", R=6, T=40, H=512 if variant == B.AR_VARIANT_WARP_ROW
+                        else 2048, dtype=dtype, pattern=W.RES_NORM)
+    inp = W.make_fused_inputs(w)
+    inp.partials = special_draw(dtype, (w.R, w.T, w.H), seed=7, finite=True)
+    for acc in (B.AR_ACC_ELEMENT, B.AR_ACC_FP32):
+        stats, _, _ = run_and_check(w, variant, False, inp=inp, acc=acc)
+        assert stats.get("residual_mismatch", 0) == 0, (acc, stats)
+        assert stats.get("norm_mismatch", 0) <= max(1, w.T * w.H // 100000), (acc, stats)
+
+
 @pytest.mark.parametrize("staged", [False, True])
 def test_staged_buffer_mode_and_capacity(staged):
     w = W.DECODE.with_(T=100)
