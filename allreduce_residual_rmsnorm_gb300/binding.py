@@ -40,7 +40,6 @@ AR_VARIANT_AUTO = 0
 AR_VARIANT_WARP_ROW = 1
 AR_VARIANT_CTA_ROW = 2
 AR_VARIANT_BULK_PIPE = 3
-AR_VARIANT_CTA_ROW_ASYNC = 4
 
 # enum ar_scale_layout
 AR_SF_LINEAR = 0

@@ -25,8 +25,6 @@ namespace arf {
 cudaError_t launch_fused_rows_bf16(int variant, const FusedArgs& a, const LaunchCfg& c);
 cudaError_t launch_fused_rows_fp16(int variant, const FusedArgs& a, const LaunchCfg& c);
 cudaError_t launch_fused_rows_fp32(int variant, const FusedArgs& a, const LaunchCfg& c);
-bool fused_rows_async_supported(int dtype, int H, int R, bool lamport);
-cudaError_t launch_fused_rows_async(int dtype, const FusedArgs& a, const LaunchCfg& c);
 
 cudaError_t launch_fused_rows(int dtype, int variant, const FusedArgs& a, const LaunchCfg& c)
 {
@@ -330,9 +328,6 @@ int pick_variant(const ar_fusion_ws* ws, const FusedArgs& a)
         v = AR_VARIANT_AUTO;
     if (v == AR_VARIANT_WARP_ROW && a.H > 1024)
         v = AR_VARIANT_AUTO;
-    if (v == AR_VARIANT_CTA_ROW_ASYNC &&
-        !fused_rows_async_supported(ws->dtype, a.H, a.R, a.lamport != 0))
-        v = AR_VARIANT_AUTO;
     if (v != AR_VARIANT_AUTO)
         return v;
     // One row per warp only up to hidden 512 (at hidden 1024 the block
@@ -388,9 +383,8 @@ int launch_fused(ar_fusion_ws* ws, const FusedArgs& a, cudaStream_t s)
     ws->last_variant = variant;
     ws->last_cluster = 1;
     c.used_cluster = &ws->last_cluster;
-    cudaError_t e = variant == AR_VARIANT_BULK_PIPE      ? launch_fused_pipe(ws->dtype, a, c)
-                    : variant == AR_VARIANT_CTA_ROW_ASYNC ? launch_fused_rows_async(ws->dtype, a, c)
-                                                          : launch_fused_rows(ws->dtype, variant, a, c);
+    cudaError_t e = variant == AR_VARIANT_BULK_PIPE ? launch_fused_pipe(ws->dtype, a, c)
+                                                    : launch_fused_rows(ws->dtype, variant, a, c);
     if (e != cudaSuccess)
         return cuda_fail(e, "fused kernel launch");
     return AR_OK;
@@ -596,7 +590,7 @@ int ar_fusion_workspace_set_timeout_ns(ar_fusion_ws* ws, uint64_t ns)
 
 int ar_fusion_workspace_set_variant(ar_fusion_ws* ws, int variant)
 {
-    if (!ws || variant < AR_VARIANT_AUTO || variant > AR_VARIANT_CTA_ROW_ASYNC)
+    if (!ws || variant < AR_VARIANT_AUTO || variant > AR_VARIANT_BULK_PIPE)
         return fail(AR_ERR_INVALID, "workspace NULL or variant %d unknown", variant);
     ws->variant = variant;
     return AR_OK;

@@ -28,7 +28,7 @@ def main(argv=None):
     from allreduce_residual_rmsnorm_gb300 import workloads as W
 
     p = argparse.ArgumentParser()
-    p.add_argument("--variant", default="auto", choices=["auto", "warp", "cta", "pipe", "async"])
+    p.add_argument("--variant", default="auto", choices=["auto", "warp", "cta", "pipe"])
     p.add_argument("--ranks", type=int, default=8)
     p.add_argument("--tokens", type=int, default=2048)
     p.add_argument("--hidden", type=int, default=7168)
@@ -65,8 +65,7 @@ def main(argv=None):
     ws = B.ar_fusion_workspace_create(w.R, w.T, w.H, dt)
     B.ar_fusion_workspace_set_variant(ws, {"auto": B.AR_VARIANT_AUTO, "warp": B.AR_VARIANT_WARP_ROW,
                                            "cta": B.AR_VARIANT_CTA_ROW,
-                                           "pipe": B.AR_VARIANT_BULK_PIPE,
-                                           "async": B.AR_VARIANT_CTA_ROW_ASYNC}[a.variant])
+                                           "pipe": B.AR_VARIANT_BULK_PIPE}[a.variant])
     B.ar_fusion_workspace_set_launch(ws, a.cluster, a.pdl)
     mode = B.AR_MODE_LAMPORT if a.lamport else B.AR_MODE_BUFFER
     B.ar_fusion_workspace_set_mode(ws, mode)

@@ -48,7 +48,7 @@ def parse():
     p.add_argument("--e2e-chunks", type=int, default=8,
                    help="row chunks of the pipelined end-to-end step (1 = no pipelining)")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--variant", default="auto", choices=["auto", "cta", "pipe", "warp", "async"])
+    p.add_argument("--variant", default="auto", choices=["auto", "cta", "pipe", "warp"])
     p.add_argument("--tokens", type=int, default=None,
                    help="smaller token count (profiling captures); default: the full workload")
     p.add_argument("--no-e2e", action="store_true")
@@ -329,8 +329,7 @@ def run_sweep(args):
         info = B.ar_fusion_workspace_info(ws)
         last = info["last_variant"]
         print(json.dumps({"sweep": w.name, "dtype": w.dtype, "mode": "lamport" if lam else "buffer",
-                          "variant": {1: "warp_row", 2: "cta_row", 3: "bulk_pipe",
-                                      4: "cta_row_async"}.get(last),
+                          "variant": {1: "warp_row", 2: "cta_row", 3: "bulk_pipe"}.get(last),
                           "cluster": cl, "cluster_used": info["last_cluster"], "pdl": pdl,
                           "us": us, "tokens_per_s": w.T / (us * 1e-6), "bytes": byts,
                           "gbs": byts / (us * 1e-6) / 1e9, "frac_of_copy_peak": byts / (us * 1e-6) / 1e9 / peak,
@@ -404,15 +403,6 @@ def run_sweep(args):
             B.ar_fusion_workspace_set_accumulate(ws, B.AR_ACC_FP32)
             B.ar_fusion_workspace_set_scale_layout(ws, B.AR_SF_LINEAR)
             del sf_swz
-        if not lam and w.dtype != "fp32" and w.R <= 8 and w.H // 8 <= (1024 if w.R <= 4 else 896):
-            # the opt-in row kernel whose threads copy the next row into shared
-            # memory, on the same staged call
-            B.ar_fusion_workspace_set_launch(ws, 0, 0)
-            B.ar_fusion_workspace_set_variant(ws, B.AR_VARIANT_CTA_ROW_ASYNC)
-            stage()
-            us = graph_us(call)
-            report(w, pat, ws, lam, us, 0, 0)
-            B.ar_fusion_workspace_set_variant(ws, B.AR_VARIANT_AUTO)
         eb = 4 if w.dtype == "fp32" else 2
         if (w.R + 3) * w.T * w.H * eb < 2 * l2_bytes:
             # caller partials (no staging), inputs evicted before every call
@@ -489,8 +479,7 @@ def main():
     stream = torch.cuda.current_stream(dev)
     ws = B.ar_fusion_workspace_create(R, T, H, B.AR_DT_BF16)
     variant = {"auto": B.AR_VARIANT_AUTO, "cta": B.AR_VARIANT_CTA_ROW,
-               "pipe": B.AR_VARIANT_BULK_PIPE, "warp": B.AR_VARIANT_WARP_ROW,
-               "async": B.AR_VARIANT_CTA_ROW_ASYNC}[args.variant]
+               "pipe": B.AR_VARIANT_BULK_PIPE, "warp": B.AR_VARIANT_WARP_ROW}[args.variant]
     B.ar_fusion_workspace_set_variant(ws, variant)
     P = inp["P"].to(dev)
     X = inp["X"].to(dev)
@@ -627,10 +616,8 @@ def main():
     achieved = bytes_alg / avg_launch_s / 1e9
     last = B.ar_fusion_workspace_info(ws)["last_variant"]
     used_variant = {B.AR_VARIANT_CTA_ROW: "cta_row", B.AR_VARIANT_BULK_PIPE: "bulk_pipe",
-                    B.AR_VARIANT_WARP_ROW: "warp_row",
-                    B.AR_VARIANT_CTA_ROW_ASYNC: "cta_row_async"}.get(last, "none")
-    kname = {B.AR_VARIANT_BULK_PIPE: "fused_pipe_kernel",
-             B.AR_VARIANT_CTA_ROW_ASYNC: "fused_rows_async_kernel"}.get(last, "fused_rows_kernel")
+                    B.AR_VARIANT_WARP_ROW: "warp_row"}.get(last, "none")
+    kname = "fused_pipe_kernel" if last == B.AR_VARIANT_BULK_PIPE else "fused_rows_kernel"
     line = {
         "metric": METRIC,
         "value": value,

@@ -132,16 +132,8 @@ enum ar_variant {
     AR_VARIANT_AUTO = 0,
     AR_VARIANT_WARP_ROW = 1,  /* one row per warp (small hidden) */
     AR_VARIANT_CTA_ROW = 2,   /* one row per thread block, loads straight to registers */
-    AR_VARIANT_BULK_PIPE = 3, /* persistent blocks, rank rows streamed into shared
+    AR_VARIANT_BULK_PIPE = 3  /* persistent blocks, rank rows streamed into shared
                                  memory by bulk async copies (large token counts) */
-    AR_VARIANT_CTA_ROW_ASYNC = 4  /* one row per thread block, each thread's vectors of
-                                     the block's next row copied into shared memory
-                                     (cp.async) while the current row is reduced;
-                                     bf16/fp16, staged buffer or caller partials,
-                                     nranks <= 8, hidden <= 7168 (<= 8192 with at
-                                     most 4 ranks).  Opt-in only; where it does not
-                                     apply (Lamport mode, fp32, wider rows, more
-                                     ranks) the call takes AUTO's choice. */
 };
 
 #define AR_MAX_RANKS 16
