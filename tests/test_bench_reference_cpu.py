@@ -44,3 +44,12 @@ def test_reference_arm_other_ranks_exit_without_work():
                   env={"RANK": "1", "LOCAL_RANK": "1", "WORLD_SIZE": "2"})
     assert r.returncode == 0, r.stderr[-2000:]
     assert not [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+
+
+def test_algorithmic_bytes_of_the_benchmarked_workload():
+    # 8 partials + residual_in + residual_out (bf16) + NVFP4 codes + E4M3 block
+    # scales of 8192 x 7168: 939,524,096 + 2 x 117,440,512 + 29,360,128 + 3,670,016
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.algorithmic_bytes(8, 8192, 7168) == 1_207_435_264
+    assert bench.algorithmic_bytes(1, 1, 16) == 16 * 2 * 3 + 8 + 1
