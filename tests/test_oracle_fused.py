@@ -307,6 +307,16 @@ def test_fp8_amax_element_maps_to_448_and_roundtrip_bound():
     assert np.all(np.signbit(n[n != 0]) == ((q[n != 0] & 0x80) != 0))
 
 
+@pytest.mark.parametrize("dtype", [BF16, FP16])
+def test_amax_is_the_largest_magnitude_on_either_side(dtype):
+    # the per-tensor scale must cover the most negative element too
+    tdt = torch.bfloat16 if dtype == BF16 else torch.float16
+    x = torch.tensor([[0.5, -3.5, 2.0, -0.0], [1.25, 0.0, -1.0, 3.0]], dtype=tdt)
+    assert oracle.amax(dtype, bits(x)) == 3.5
+    assert oracle.amax(dtype, bits(-x)) == 3.5
+    assert oracle.amax(dtype, bits(torch.zeros(3, 8, dtype=tdt))) == 0.0
+
+
 # ------------------------------------------------------------------ NVFP4
 
 def test_scales_of_an_all_zero_tensor_are_finite():

@@ -76,10 +76,23 @@ MUTANTS = {
                                "float enc = (dec == 0.0f) ? 0.0f : dec / gs;", 1),
     "f32_sum_subtract": ("s = s + in[(int64_t)r * rank_stride + i];", "s = s - in[(int64_t)r * rank_stride + i];"),
     "buffer_size_missing_R": ("out[0] = (int64_t)R * max_tokens * H * elem_bytes;", "out[0] = max_tokens * H * elem_bytes;"),
+    "f16_subnormal_decode_scale": ("mag = (float)m * 0x1p-24f;", "mag = (float)m * 0x1p-25f;"),
+    "e4m3_decode_bias": ("mag = ldexpf(1.0f + (float)m / 8.0f, e - 7);",
+                         "mag = ldexpf(1.0f + (float)m / 8.0f, e - 8);"),
+    "amax_no_abs": ("m = fmaxf(m, fabsf(dec_d(dtype, x[i])));", "m = fmaxf(m, dec_d(dtype, x[i]));"),
+    "nvfp4_block_max_no_abs": ("bmax = fmaxf(bmax, fabsf(dec_d(dtype, blk[i])));",
+                               "bmax = fmaxf(bmax, dec_d(dtype, blk[i]));"),
+    "sum_of_abs_not_squares": ("ss += yd * yd;", "ss += fabs(yd);"),
+    "swizzle_row_major_inside_tile": ("int64_t within = (m % 32) * 16 + ((m / 32) % 4) * 4 + k % 4;",
+                                      "int64_t within = (m % 32) * 4 + ((m / 32) % 4) * 128 + k % 4;"),
+    "swizzle_tiles_column_major": ("int64_t tile = (m / 128) * ktiles + k / 4;",
+                                   "int64_t tile = (k / 4) * ((T + 127) / 128) + m / 128;"),
 }
 
 PINS = [
     C.test_bf16_round_matches_torch, C.test_f16_round_matches_numpy,
+    C.test_bf16_decode_matches_torch, C.test_f16_decode_matches_numpy,
+    C.test_e4m3_decode_facts, C.test_e4m3_decode_matches_torch, C.test_e2m1_decode_table,
     C.test_e4m3_encode_matches_torch_below_saturation, C.test_e4m3_saturates_and_keeps_nan,
     C.test_e4m3_ties_to_even_examples,
     C.test_e2m1_encode_brute_force, C.test_e2m1_ties_to_even_examples,
@@ -95,6 +108,7 @@ PINS = [
     Fz.test_norm_invariant_locates_eps_and_mean,
     Fz.test_lamport_flip_only_touches_negative_zero_words,
     Fz.test_fp8_amax_element_maps_to_448_and_roundtrip_bound,
+    lambda: Fz.test_amax_is_the_largest_magnitude_on_either_side(oracle.BF16),
     Fz.test_nvfp4_zero_block_and_max_element,
     Fz.test_nvfp4_nibble_order_convention,
     Fz.test_nvfp4_roundtrip_bound_random,
@@ -102,6 +116,11 @@ PINS = [
     Fz.test_element_type_accumulation_worked_value,
     lambda: Fz.test_element_type_accumulation_is_chained_library_adds(oracle.BF16),
     Fz.test_vector_sum_element_type_accumulation,
+    lambda: Fz.test_vector_sum_element_type_special_values_are_chained_library_adds(oracle.FP16),
+    Fz.test_scales_of_an_all_zero_tensor_are_finite,
+    Fz.test_swizzled_scales_worked_positions,
+    lambda: [Fz.test_swizzled_scales_are_a_tile_permutation(T, KB)
+             for T, KB in ((128, 4), (257, 448), (300, 5))],
     Fz.test_workspace_sizes_match_page_formula_golden,
     Fz.test_lamport_state_cycles,
     lambda: [Fz.test_f32_identical_partials_power_of_two_ranks(R) for R in (2, 8)],
