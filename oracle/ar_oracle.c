@@ -412,8 +412,8 @@ void oracle_sum(int dtype, int acc, int R, int64_t n, int64_t rank_stride, const
  * creation's use_fp32_lamport: the exchanged buffers hold fp32).  Every
  * rounding to the element type of the 16-bit path is the identity here:
  *   s = P_0 + ... + P_{R-1} (fp32, rank order);  y = s + X   -> residual_out
- *   ss = sum_h y_h^2 in fp64 (exact: 24-bit significands square into 48 bits),
- *        rounded once to fp32;  rstd = 1 / sqrt(ss / H + eps)
+ *   ss = sum_h y_h^2 in fp64 (each square exact: 24-bit significands square
+ *        into 48 bits), rounded once to fp32;  rstd = 1 / sqrt(ss / H + eps)
  *   n = (y * rstd) * gamma                                    -> norm_out
  * Arrays as in oracle_fused_rows, of float. */
 void oracle_fused_rows_f32(int R, int64_t T, int64_t H, int64_t rank_stride,

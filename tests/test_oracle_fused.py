@@ -248,6 +248,110 @@ def test_exact_rational_brute_force_tiny():
             assert d.max() <= 1, (trial, t)
 
 
+# Exact rational arithmetic with explicit round-to-nearest-even, for pins that
+# must see every fp32 rounding of the normalisation in the pages' order.
+F32_BITS, F16_BITS, BF16_BITS = 23, 10, 7
+
+
+def _rnd(q, mbits):
+    """q rounded to nearest (ties to even) with `mbits` fraction bits (normal range)."""
+    if q == 0:
+        return Fraction(0)
+    sgn = -1 if q < 0 else 1
+    a = abs(Fraction(q))
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    quantum = Fraction(2) ** (e - mbits)
+    n = a / quantum
+    fl = n.numerator // n.denominator
+    rem = n - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    return sgn * fl * quantum
+
+
+def _sqrt_rnd32(q):
+    """Correctly rounded fp32 square root of a positive rational."""
+    q = Fraction(q)
+    e = (q.numerator.bit_length() - q.denominator.bit_length()) // 2
+    while Fraction(4) ** e > q:
+        e -= 1
+    while Fraction(4) ** (e + 1) <= q:
+        e += 1
+    quantum = Fraction(2) ** (e - F32_BITS)
+    n = q / (quantum * quantum)                  # sqrt(n) in [2^23, 2^24)
+    fl = math.isqrt(n.numerator // n.denominator)
+    mid = Fraction(2 * fl + 1, 2) ** 2
+    if n > mid or (n == mid and fl % 2 == 1):
+        fl += 1
+    return fl * quantum
+
+
+def _exact_row(P, x, g, eps, mbits):
+    """One row in the pages' order, every step rounded as stated: fp32 rank
+    sum, rounded to D; fp32 residual add, rounded to D; sum of squares exact,
+    rounded to fp32 once; mean = ss / H; + eps; sqrt; 1 / sqrt (each fp32);
+    n = ((y * rstd) * gamma) left to right in fp32, rounded to D."""
+    H = len(x)
+    eps32 = _rnd(Fraction(eps), F32_BITS)
+    y = []
+    for h in range(H):
+        s = Fraction(float(P[0][h]))
+        for r in range(1, len(P)):
+            s = _rnd(s + Fraction(float(P[r][h])), F32_BITS)
+        a = _rnd(s, mbits)
+        y.append(_rnd(_rnd(a + Fraction(float(x[h])), F32_BITS), mbits))
+    ss32 = _rnd(sum(v * v for v in y), F32_BITS)
+    ms = _rnd(ss32 / H, F32_BITS)
+    v = _rnd(ms + eps32, F32_BITS)
+    rstd = _rnd(1 / _sqrt_rnd32(v), F32_BITS)
+    n = [_rnd(_rnd(_rnd(yh * rstd, F32_BITS) * Fraction(float(g[h])), F32_BITS), mbits)
+         for h, yh in enumerate(y)]
+    return y, rstd, n
+
+
+@pytest.mark.parametrize("dtype", [BF16, FP16])
+def test_rows_follow_the_pages_rounding_order_exactly(dtype):
+    # Random rows (hidden sizes that are not powers of two, so dividing by H
+    # rounds): residual_out, the fp32 rstd and norm_out equal the exact
+    # step-by-step evaluation bit for bit.
+    tdt = torch.bfloat16 if dtype == BF16 else torch.float16
+    mbits = BF16_BITS if dtype == BF16 else F16_BITS
+    g = torch.Generator().manual_seed(21 + dtype)
+    for R, H, eps in ((1, 24, 1e-6), (2, 40, 1e-5), (3, 56, 0.01), (2, 200, 0.3), (4, 96, 1e-6)):
+        T = 3
+        P = torch.randn(R, T, H, generator=g).to(tdt)
+        X = torch.randn(T, H, generator=g).to(tdt)
+        G = (1 + 0.3 * torch.randn(H, generator=g)).to(tdt)
+        res, nrm, rstd = run(P, X, G, eps, dtype)
+        for t in range(T):
+            y, r32, n = _exact_row(P[:, t].float().numpy(), X[t].float().numpy(),
+                                   G.float().numpy(), eps, mbits)
+            assert np.array_equal(res[t], bits(torch.tensor([float(v) for v in y]).to(tdt)))
+            assert Fraction(float(rstd[t])) == r32, (R, H, t)
+            assert np.array_equal(nrm[t], bits(torch.tensor([float(v) for v in n]).to(tdt)))
+
+
+def test_normalisation_multiplies_rstd_before_gamma():
+    # A constant fp16 row where the two product orders round to different
+    # fp16 values: y = 1.8515625 (all 8 elements), eps = 0.0399933..., gamma_0
+    # = 0.35888671875.  (y * rstd) * gamma gives 0.356689453125; (y * gamma)
+    # * rstd would give 0.3569335... (one fp16 step higher).
+    c, eps, g0 = 1.8515625, 0.03999330475926399, 0.35888671875
+    H = 8
+    P = torch.zeros(1, 1, H, dtype=torch.float16)
+    X = torch.full((1, H), c, dtype=torch.float16)
+    G = torch.ones(H, dtype=torch.float16)
+    G[0] = g0
+    _, nrm, _ = run(P, X, G, eps, FP16)
+    _, rstd, n = _exact_row(P[:, 0].float().numpy(), X[0].float().numpy(), G.float().numpy(),
+                            eps, F16_BITS)
+    other = _rnd(_rnd(_rnd(Fraction(c) * Fraction(g0), F32_BITS) * rstd, F32_BITS), F16_BITS)
+    assert n[0] == Fraction(0.356689453125) and other != n[0]
+    assert nrm[0][0] == bits(torch.tensor([0.356689453125], dtype=torch.float16))[0]
+
+
 def test_norm_invariant_locates_eps_and_mean():
     # mean_h (n_h / gamma_h)^2 = ms / (ms + eps) up to bf16 rounding; a large
     # eps makes the factor far from 1 so a misplaced eps or a wrong divisor
@@ -532,6 +636,24 @@ def test_f32_constant_row_with_eps_closed_form():
     out, nrm, rstd = run32(P, torch.full((3, 1024), 0.25), gamma, 0.4375)
     assert np.all(out == np.float32(0.75)) and np.all(rstd == np.float32(1.0))
     assert np.array_equal(nrm, (0.75 * gamma).expand(3, 1024).numpy())
+
+
+def test_f32_rows_follow_the_pages_rounding_order_exactly():
+    # fp32 elements: every rounding of the row is an fp32 rounding and none is
+    # hidden by a final 16-bit one, so residual_out, rstd and norm_out are
+    # compared bit for bit with the exact step-by-step evaluation
+    g = torch.Generator().manual_seed(31)
+    for R, H, eps in ((1, 24, 1e-6), (2, 40, 1e-5), (3, 200, 0.25), (4, 56, 1e-6)):
+        T = 3
+        P = torch.randn(R, T, H, generator=g)
+        X = torch.randn(T, H, generator=g)
+        G = 1 + 0.3 * torch.randn(H, generator=g)
+        res, nrm, rstd = run32(P, X, G, eps)
+        for t in range(T):
+            y, r32, n = _exact_row(P[:, t].numpy(), X[t].numpy(), G.numpy(), eps, F32_BITS)
+            assert [Fraction(float(v)) for v in res[t]] == y, (R, H, t)
+            assert Fraction(float(rstd[t])) == r32, (R, H, t)
+            assert [Fraction(float(v)) for v in nrm[t]] == n, (R, H, t)
 
 
 def test_f32_norm_is_rmsnorm_of_residual_out():

@@ -85,6 +85,16 @@ MUTANTS = {
     "sum_of_abs_not_squares": ("ss += yd * yd;", "ss += fabs(yd);"),
     "swizzle_row_major_inside_tile": ("int64_t within = (m % 32) * 16 + ((m / 32) % 4) * 4 + k % 4;",
                                       "int64_t within = (m % 32) * 4 + ((m / 32) % 4) * 128 + k % 4;"),
+    "norm_gamma_before_rstd": ("float ny = dec_d(dtype, y) * rstd;\n            float n = ny * dec_d(dtype, gamma[h]);",
+                               "float ny = dec_d(dtype, y) * dec_d(dtype, gamma[h]);\n            float n = ny * rstd;"),
+    "mean_in_fp64": ("float ms = ss32 / (float)H;", "float ms = (float)(ss / (double)H);", 0),
+    "mean_by_reciprocal": ("float ms = ss32 / (float)H;", "float ms = ss32 * (1.0f / (float)H);", 0),
+    "nvfp4_enc_unrounded_scale": ("float enc = (dec == 0.0f) ? 0.0f : gs / dec;",
+                                  "float enc = (dec == 0.0f) ? 0.0f : 6.0f / bmax;", 0),
+    "f32_norm_gamma_before_rstd": ("float ny = y * rstd;\n            norm_out[t * H + h] = ny * gamma[h];",
+                                   "float ny = y * gamma[h];\n            norm_out[t * H + h] = ny * rstd;"),
+    "f32_mean_in_fp64": ("float ms = ss32 / (float)H;", "float ms = (float)(ss / (double)H);", 1),
+    "f32_mean_by_reciprocal": ("float ms = ss32 / (float)H;", "float ms = ss32 * (1.0f / (float)H);", 1),
     "swizzle_tiles_column_major": ("int64_t tile = (m / 128) * ktiles + k / 4;",
                                    "int64_t tile = (k / 4) * ((T + 127) / 128) + m / 128;"),
 }
@@ -106,6 +116,8 @@ PINS = [
     Fz.test_constant_row_with_eps_closed_form,
     Fz.test_exact_rational_brute_force_tiny,
     Fz.test_norm_invariant_locates_eps_and_mean,
+    lambda: Fz.test_rows_follow_the_pages_rounding_order_exactly(oracle.FP16),
+    Fz.test_normalisation_multiplies_rstd_before_gamma,
     Fz.test_lamport_flip_only_touches_negative_zero_words,
     Fz.test_fp8_amax_element_maps_to_448_and_roundtrip_bound,
     lambda: Fz.test_amax_is_the_largest_magnitude_on_either_side(oracle.BF16),
@@ -129,6 +141,7 @@ PINS = [
     Fz.test_f32_constant_power_of_two_row,
     Fz.test_f32_constant_row_with_eps_closed_form,
     Fz.test_f32_norm_is_rmsnorm_of_residual_out,
+    Fz.test_f32_rows_follow_the_pages_rounding_order_exactly,
     Fz.test_f32_quantisers_match_the_16_bit_ones_on_representable_values,
     Fz.test_f32_vector_sum,
 ]
