@@ -36,8 +36,11 @@
  * Parity pins for every function live in tests/test_oracle_*.py.  The NVFP4
  * global-scale convention (gs = 2688 / amax, enc = gs / f(sf)) is a stated
  * reading (the quantiser's helper header is not on the pages): parity
- * unpinned for that convention only.  The block-scale tile layout is pinned
- * outside the oracle, by a block-scaled matmul library reading it.
+ * unpinned for that convention only -- a property pin holds the oracle to the
+ * reading (the amax block gets the largest block scale, 448, and its largest
+ * element the code +-6), but nothing outside it fixes the reading itself.
+ * The block-scale tile layout is pinned outside the oracle, by a
+ * block-scaled matmul library reading it.
  */
 #include <math.h>
 #include <stdint.h>

@@ -451,6 +451,27 @@ def test_nvfp4_zero_block_and_max_element():
     assert codes1[15] == 0xf
 
 
+@pytest.mark.parametrize("dtype", [BF16, FP16])
+def test_nvfp4_global_scale_puts_the_amax_block_on_the_largest_scale(dtype):
+    # The stated global-scale convention (the tensor amax maps onto 448 x 6,
+    # the largest E4M3 block scale times the largest E2M1 value) is a reading,
+    # not on the pages; this holds the oracle to it: the block holding the
+    # amax gets scale byte 0x7E (448) and its largest element the code +-6.
+    nrm = _norm_of_random(seed=17) if dtype == BF16 else bits(
+        torch.from_numpy(_norm_of_random(seed=17).view(np.int16)).view(torch.bfloat16)
+        .float().to(torch.float16))
+    tdt = torch.bfloat16 if dtype == BF16 else torch.float16
+    n = torch.from_numpy(nrm.view(np.int16)).view(tdt).float().numpy()
+    amax = oracle.amax(dtype, nrm)
+    q, sf = oracle.quant_nvfp4(dtype, nrm, oracle.nvfp4_global_scale(amax))
+    t, h = np.argwhere(np.abs(n) == amax)[0]
+    assert sf[t, h // 16] == 0x7E
+    code = (q[t, h // 2] >> (4 * (h % 2))) & 0xF
+    assert code == (0xF if n[t, h] < 0 else 0x7)
+    # no block scale exceeds it
+    assert sf.max() <= 0x7E
+
+
 def test_nvfp4_nibble_order_convention():
     # Stated convention: element 2k in the low nibble of byte k.
     n = np.zeros((1, 16), np.uint16)

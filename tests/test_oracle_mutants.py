@@ -95,6 +95,15 @@ MUTANTS = {
                                    "float ny = y * gamma[h];\n            norm_out[t * H + h] = ny * rstd;"),
     "f32_mean_in_fp64": ("float ms = ss32 / (float)H;", "float ms = (float)(ss / (double)H);", 1),
     "f32_mean_by_reciprocal": ("float ms = ss32 / (float)H;", "float ms = ss32 * (1.0f / (float)H);", 1),
+    "nvfp4_global_scale_448": ("return 2688.0f / amax;", "return 448.0f / amax;"),
+    "nvfp4_sf_index_transposed": ("scale_out[t * (H / 16) + b] = sf;",
+                                  "scale_out[(b * T + t) % (T * (H / 16))] = sf;", 0),
+    "nvfp4_block_max_of_8": ("for (int i = 0; i < 16; ++i)\n                bmax = fmaxf(bmax, fabsf(dec_d(dtype, blk[i])));",
+                             "for (int i = 0; i < 8; ++i)\n                bmax = fmaxf(bmax, fabsf(dec_d(dtype, blk[i])));"),
+    "fp8_divides_by_inverse_scale": ("q[i] = oracle_f32_to_e4m3(dec_d(dtype, n_in[i]) * inv_scale);",
+                                     "q[i] = oracle_f32_to_e4m3(dec_d(dtype, n_in[i]) / inv_scale);"),
+    "flip_any_negative_zero_half": ("if (words[i] == 0x80000000u)",
+                                    "if ((words[i] & 0xffffu) == 0x8000u || (words[i] >> 16) == 0x8000u)"),
     "swizzle_tiles_column_major": ("int64_t tile = (m / 128) * ktiles + k / 4;",
                                    "int64_t tile = (k / 4) * ((T + 127) / 128) + m / 128;"),
 }
@@ -122,6 +131,7 @@ PINS = [
     Fz.test_fp8_amax_element_maps_to_448_and_roundtrip_bound,
     lambda: Fz.test_amax_is_the_largest_magnitude_on_either_side(oracle.BF16),
     Fz.test_nvfp4_zero_block_and_max_element,
+    lambda: Fz.test_nvfp4_global_scale_puts_the_amax_block_on_the_largest_scale(oracle.BF16),
     Fz.test_nvfp4_nibble_order_convention,
     Fz.test_nvfp4_roundtrip_bound_random,
     Fz.test_vector_sum_closed_form_and_fp64,
