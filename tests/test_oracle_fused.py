@@ -393,6 +393,20 @@ def _norm_of_random(T=16, H=256, seed=9):
     return nrm
 
 
+def test_fp8_multiplier_is_the_reciprocal_of_the_rounded_scale():
+    # The configuration supplies scale = amax / 448 and the kernel multiplies
+    # by its inverse: two fp32 roundings, rnd(1 / rnd(amax / 448)), which for
+    # some amax differs from the single rounding of 448 / amax.
+    amaxes = torch.linspace(0.01, 300.0, 3001).to(torch.bfloat16).float().unique().numpy()
+    differs = 0
+    for a in amaxes:
+        want = _rnd(1 / _rnd(Fraction(float(a)) / 448, F32_BITS), F32_BITS)
+        assert Fraction(float(oracle.fp8_inv_scale(float(a)))) == want, a
+        differs += want != _rnd(Fraction(448) / Fraction(float(a)), F32_BITS)
+    assert differs > 0
+    assert oracle.fp8_inv_scale(0.0) == 1.0
+
+
 def test_fp8_amax_element_maps_to_448_and_roundtrip_bound():
     nrm = _norm_of_random()
     amax = oracle.amax(BF16, nrm)

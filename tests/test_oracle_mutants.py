@@ -104,6 +104,12 @@ MUTANTS = {
                                      "q[i] = oracle_f32_to_e4m3(dec_d(dtype, n_in[i]) / inv_scale);"),
     "flip_any_negative_zero_half": ("if (words[i] == 0x80000000u)",
                                     "if ((words[i] & 0xffffu) == 0x8000u || (words[i] >> 16) == 0x8000u)"),
+    "fp8_inv_scale_one_division": ("return 1.0f / scale;", "return 448.0f / amax;"),
+    "e4m3_binade_carry_missing": ("if (n == 16u) { n = 8u; e += 1; }", "if (n == 16u) { n = 15u; }"),
+    "e2m1_binade_carry_missing": ("if (n == 4u) { n = 2u; e += 1; }", "if (n == 4u) { n = 3u; }"),
+    "e4m3_sign_of_zero_lost": ("uint8_t s = (uint8_t)((f2u(x) >> 24) & 0x80u);",
+                               "uint8_t s = (uint8_t)(x < 0.0f ? 0x80u : 0u);"),
+    "lamport_clear_size_missing_R": ("io[1] = (int64_t)R * T * H;", "io[1] = (int64_t)T * H;"),
     "swizzle_tiles_column_major": ("int64_t tile = (m / 128) * ktiles + k / 4;",
                                    "int64_t tile = (k / 4) * ((T + 127) / 128) + m / 128;"),
 }
@@ -129,6 +135,7 @@ PINS = [
     Fz.test_normalisation_multiplies_rstd_before_gamma,
     Fz.test_lamport_flip_only_touches_negative_zero_words,
     Fz.test_fp8_amax_element_maps_to_448_and_roundtrip_bound,
+    Fz.test_fp8_multiplier_is_the_reciprocal_of_the_rounded_scale,
     lambda: Fz.test_amax_is_the_largest_magnitude_on_either_side(oracle.BF16),
     Fz.test_nvfp4_zero_block_and_max_element,
     lambda: Fz.test_nvfp4_global_scale_puts_the_amax_block_on_the_largest_scale(oracle.BF16),
