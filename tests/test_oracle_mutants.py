@@ -110,6 +110,13 @@ MUTANTS = {
     "e4m3_sign_of_zero_lost": ("uint8_t s = (uint8_t)((f2u(x) >> 24) & 0x80u);",
                                "uint8_t s = (uint8_t)(x < 0.0f ? 0x80u : 0u);"),
     "lamport_clear_size_missing_R": ("io[1] = (int64_t)R * T * H;", "io[1] = (int64_t)T * H;"),
+    "slot_ignores_oneshot_floor": ("int64_t tok = max_tokens > oneshot_max ? max_tokens : oneshot_max;",
+                                   "int64_t tok = max_tokens;"),
+    "flag_bytes_without_R": ("out[1] = (int64_t)R * flag_count * 4;", "out[1] = flag_count * 4;"),
+    "two_lamport_slots": ("out[3] = 3 * out[2];", "out[3] = 2 * out[2];"),
+    "lamport_reads_wrong_slot": ("io[2] = flag % 3;", "io[2] = (flag + 1) % 3;"),
+    "f32_sf_index_transposed": ("scale_out[t * (H / 16) + b] = sf;",
+                                "scale_out[(b * T + t) % (T * (H / 16))] = sf;", 1),
     "swizzle_tiles_column_major": ("int64_t tile = (m / 128) * ktiles + k / 4;",
                                    "int64_t tile = (k / 4) * ((T + 127) / 128) + m / 128;"),
 }
