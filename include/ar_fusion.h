@@ -222,10 +222,11 @@ int ar_fusion_workspace_create(int tp_size, int max_token_num, int hidden_dim, i
  * NULL is accepted (no-op). */
 int ar_fusion_workspace_destroy(ar_fusion_ws* ws);
 
-/* Fill *info.  No CUDA call. */
+/* Fill *info.  No CUDA call.  Errors: AR_ERR_INVALID for a NULL argument. */
 int ar_fusion_workspace_info(const ar_fusion_ws* ws, ar_fusion_ws_info* info);
 
-/* Copy the device state block to host memory *out (synchronises `stream`). */
+/* Copy the device state block to host memory *out (synchronises `stream`).
+ * Errors: AR_ERR_INVALID for a NULL argument, AR_ERR_CUDA if the copy fails. */
 int ar_fusion_workspace_copy_state(ar_fusion_ws* ws, void* stream, ar_fusion_state* out);
 
 /* Synchronise `stream`, read the device status word: returns AR_OK, the
@@ -249,7 +250,10 @@ int ar_fusion_workspace_set_timeout_ns(ar_fusion_ws* ws, uint64_t ns);
 
 /* Force a kernel variant (enum ar_variant) or staged-read mode (enum
  * ar_mode) for later calls on this workspace; AUTO restores the default
- * choice.  Host-side settings; no CUDA call. */
+ * choice.  A forced variant that cannot run a call (the bulk-copy pipe in
+ * Lamport mode, one row per warp above hidden 1024) falls back to AUTO's
+ * choice for that call.  Host-side settings; no CUDA
+ * call.  Errors: AR_ERR_INVALID for a NULL workspace or an unknown value. */
 int ar_fusion_workspace_set_variant(ar_fusion_ws* ws, int variant);
 int ar_fusion_workspace_set_mode(ar_fusion_ws* ws, int mode);
 
