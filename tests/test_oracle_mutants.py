@@ -8,6 +8,7 @@ The committed oracle is untouched.
 import os
 import subprocess
 
+import numpy as np
 import pytest
 
 import oracle
@@ -210,3 +211,38 @@ def test_pins_catch_planted_mistake(name, tmp_path, monkeypatch):
         except AssertionError:
             caught.append(getattr(pin, "__name__", "lambda"))
     assert caught, f"no pin caught mutant {name}"
+
+
+def test_pins_catch_a_dropped_row_in_the_thread_split(monkeypatch):
+    # the Python layer splits rows (elements) over threads; a split that
+    # loses the last row of a span must fail a pin
+    orig = OM._chunks
+
+    def drop_last(n, parts):
+        spans = orig(n, parts)
+        if spans and spans[-1][1] > spans[-1][0]:
+            spans[-1] = (spans[-1][0], spans[-1][1] - 1)
+        return spans
+
+    monkeypatch.setattr(OM, "_chunks", drop_last)
+    caught = []
+    for pin in PINS:
+        try:
+            pin()
+        except AssertionError:
+            caught.append(pin)
+    assert caught
+
+
+def test_results_do_not_depend_on_the_thread_count():
+    from allreduce_residual_rmsnorm_gb300 import workloads as W
+    w = W.FusedWorkload("threads", R=3, T=37, H=1024, pattern=W.RES_NORM_NVFP4, heavy_frac=0.01)
+    inp = W.make_fused_inputs(w)
+    args = (oracle.BF16, W.bits(inp.partials), W.bits(inp.residual), W.bits(inp.gamma), w.eps)
+    ref = oracle.fused(*args, threads=1)
+    for k in (2, 5, 16):
+        got = oracle.fused(*args, threads=k)
+        assert all(np.array_equal(a, b) for a, b in zip(ref, got)), k
+    x = W.make_sum_inputs(W.SumWorkload("s", R=4, N=10_007))
+    s1 = oracle.vector_sum(oracle.FP16, W.bits(x), threads=1)
+    assert np.array_equal(s1, oracle.vector_sum(oracle.FP16, W.bits(x), threads=7))
