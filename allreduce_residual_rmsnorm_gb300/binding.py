@@ -87,7 +87,7 @@ class WsInfo(ctypes.Structure):
 class State(ctypes.Structure):
     _fields_ = [
         ("counter", ctypes.c_uint32), ("flag", ctypes.c_uint32),
-        ("lamport_flag", ctypes.c_uint32), ("pad0", ctypes.c_uint32),
+        ("lamport_flag", ctypes.c_uint32), ("clear_elem_bytes", ctypes.c_uint32),
         ("comm_size", ctypes.c_uint64), ("clear_size", ctypes.c_uint64),
         ("status", ctypes.c_int32), ("detail", ctypes.c_int32), ("calls", ctypes.c_uint64),
     ]
@@ -136,6 +136,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.ar_fusion_sum.argtypes = [ctypes.POINTER(_vp), _i, ctypes.c_size_t, _i, _vp, _vp]
     L.ar_fusion_run_noalloc.argtypes = [ctypes.POINTER(_vp), _i, _i, _i, _i, _vp, _vp,
                                         ctypes.c_float, _i, _vp, _vp, _vp, _vp, _vp, _vp]
+    L.ar_fusion_noalloc_status.argtypes = [_vp, ctypes.POINTER(_i)]
     for name in ("ar_fusion_workspace_bytes", "ar_fusion_workspace_create",
                  "ar_fusion_workspace_destroy", "ar_fusion_workspace_info",
                  "ar_fusion_workspace_copy_state", "ar_fusion_workspace_status",
@@ -146,7 +147,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                  "ar_fusion_sum_ex",
                  "ar_fusion_workspace_stage", "ar_fusion_workspace_partial_ptr",
                  "ar_fusion_run", "ar_fusion_norm_amax",
-                 "ar_fusion_sum", "ar_fusion_run_noalloc"):
+                 "ar_fusion_sum", "ar_fusion_run_noalloc", "ar_fusion_noalloc_status"):
         getattr(L, name).restype = _i
     _lib = L
     return L
@@ -381,3 +382,14 @@ def ar_fusion_run_noalloc(partials, residual_in: torch.Tensor, gamma: torch.Tens
                                        ctypes.c_float(eps), pattern, _ptr(residual_out),
                                        _ptr(norm_out), _ptr(quant_out), _ptr(scale_out),
                                        _ptr(scale_factor), _stream(stream)))
+
+
+def ar_fusion_noalloc_status(stream=None):
+    """(status, detail) of the no-allocation call on the current device: the
+    first device-side error since the previous query (AR_OK if none), which
+    the query clears.  Synchronises the stream."""
+    d = ctypes.c_int(-1)
+    rc = lib().ar_fusion_noalloc_status(_stream(stream), ctypes.byref(d))
+    if rc not in (AR_OK, AR_ERR_TIMEOUT):
+        _check(rc)
+    return rc, d.value

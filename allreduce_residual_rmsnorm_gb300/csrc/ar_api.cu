@@ -126,7 +126,7 @@ __global__ void init_state_kernel(ar_fusion_state* st, uint64_t comm_size)
     st->counter = 0;
     st->flag = 0;
     st->lamport_flag = 0;
-    st->pad0 = 0;
+    st->clear_elem_bytes = 0;
     st->comm_size = comm_size;
     st->clear_size = 0;
     st->status = 0;

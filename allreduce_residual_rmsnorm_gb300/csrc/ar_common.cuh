@@ -377,8 +377,10 @@ __device__ __forceinline__ void st_u2(void* p, uint32_t a, uint32_t b)
     *reinterpret_cast<uint2*>(p) = make_uint2(a, b);
 }
 
-// -0.0f sentinel test of TensorRT-LLM allReduceFusionKernels.cu (is_neg_zero):
-// a 32-bit word equal to 0x80000000 means "not yet written".
+// Lamport sentinel (page "TensorRT-LLMs/cpp/tensorrt_llm/kernels/
+// allReduceFusionKernels.cu", the one-shot Lamport kernel): a slot word whose
+// 32 bits are those of -0.0f has not been written by its producer yet; true
+// if any word of the vector is such a word.
 __device__ __forceinline__ bool has_sentinel(const uint4& v)
 {
     return (v.x == 0x80000000u) | (v.y == 0x80000000u) | (v.z == 0x80000000u) |

@@ -16,6 +16,7 @@
 // cudaGetSymbolAddress and passed to the kernels.
 #include <cuda_runtime.h>
 #include <stdarg.h>
+#include <stddef.h>
 #include <stdio.h>
 #include <string.h>
 
@@ -57,7 +58,7 @@ __global__ void noalloc_init_kernel(uint8_t* scratch)
         st->counter = 0;
         st->flag = 0;
         st->lamport_flag = 0;
-        st->pad0 = 0;
+        st->clear_elem_bytes = 0;
         st->comm_size = kSlotBytes;
         st->clear_size = 0;
         st->status = 0;
@@ -67,8 +68,9 @@ __global__ void noalloc_init_kernel(uint8_t* scratch)
 }
 
 // Copy the caller's R partials into the current slot (lamport_flag % 3, rank r
-// at r * plane bytes) with every -0.0f word written as +0.0f; clears the
-// status word, which must start each call at zero.
+// at r * plane bytes) with every -0.0f word written as +0.0f.  The status word
+// is left alone: a device-side error stays recorded until
+// ar_fusion_noalloc_status reads and clears it.
 __global__ void noalloc_stage_kernel(arf::FusedArgs a, uint8_t* scratch, uint64_t plane_vecs)
 {
     ar_fusion_state* st = reinterpret_cast<ar_fusion_state*>(scratch + kStateOff);
@@ -84,10 +86,6 @@ __global__ void noalloc_stage_kernel(arf::FusedArgs a, uint8_t* scratch, uint64_
         v.z = v.z == 0x80000000u ? 0u : v.z;
         v.w = v.w == 0x80000000u ? 0u : v.w;
         slot[i] = v;
-    }
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-        st->status = 0;
-        st->detail = -1;
     }
 }
 
@@ -240,6 +238,44 @@ int ar_fusion_run_noalloc(const void* const* partials, int nranks, int tokens, i
     if (e != cudaSuccess)
         return nfail(AR_ERR_CUDA, "fused kernel launch: %s", cudaGetErrorString(e));
     return AR_OK;
+}
+
+int ar_fusion_noalloc_status(void* stream, int* detail)
+{
+    if (detail)
+        *detail = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return nfail(AR_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices)
+        return nfail(AR_ERR_UNSUPPORTED, "device %d beyond %d", dev, kMaxDevices);
+    uint8_t* scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_setup_mu);
+        scratch = g_scratch_ptr[dev];
+    }
+    if (!scratch)
+        return AR_OK;  // no call has run on this device yet
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t word[2] = {0, -1};  // status, detail
+    uint8_t* at = scratch + kStateOff + offsetof(ar_fusion_state, status);
+    e = cudaMemcpyAsync(word, at, sizeof word, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess)
+        return nfail(AR_ERR_CUDA, "reading the scratch status: %s", cudaGetErrorString(e));
+    if (word[0] != AR_OK) {
+        static const int32_t clean[2] = {0, -1};
+        e = cudaMemcpyAsync(at, clean, sizeof clean, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess)
+            e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess)
+            return nfail(AR_ERR_CUDA, "clearing the scratch status: %s", cudaGetErrorString(e));
+    }
+    if (detail)
+        *detail = word[1];
+    return word[0];
 }
 
 }  // extern "C"

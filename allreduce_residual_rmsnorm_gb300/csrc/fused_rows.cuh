@@ -150,10 +150,15 @@ fused_rows_kernel(const FusedArgs a)
     if (a.lamport) {
         flag = *reinterpret_cast<volatile uint32_t*>(&a.state->lamport_flag);
         const uint64_t clear_elems = *reinterpret_cast<volatile uint64_t*>(&a.state->clear_size);
+        const uint32_t clear_eb = *reinterpret_cast<volatile uint32_t*>(&a.state->clear_elem_bytes);
         slot = a.lamport_base + (size_t)(flag % 3u) * a.slot_bytes;
-        // refill the retired slot with the sentinel (clear loop of the one-shot kernel)
+        // refill the retired slot with the sentinel (clear loop of the one-shot
+        // kernel) over the bytes its last user wrote: that call's element size,
+        // which need not be this call's (never beyond the slot)
         uint8_t* clr = a.lamport_base + (size_t)((flag + 2u) % 3u) * a.slot_bytes;
-        const uint64_t nvec = clear_elems * EB / 16;
+        uint64_t nvec = clear_elems * clear_eb / 16;
+        if (nvec > a.slot_bytes / 16)
+            nvec = a.slot_bytes / 16;
         const uint64_t nth = (uint64_t)gridDim.x * blockDim.x;
         const uint4 sent = make_uint4(0x80000000u, 0x80000000u, 0x80000000u, 0x80000000u);
         for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += nth)
@@ -352,6 +357,7 @@ fused_rows_kernel(const FusedArgs a)
             if (prev == gridDim.x - 1) {
                 a.state->lamport_flag = (flag + 1u) % 3u;
                 a.state->clear_size = (uint64_t)R * a.T * H;
+                a.state->clear_elem_bytes = EB;
                 a.state->calls += 1;
                 a.state->counter = 0;
             }

@@ -181,7 +181,8 @@ typedef struct ar_fusion_state {
     uint32_t counter;        /* blocks finished in the current launch (0 between calls) */
     uint32_t flag;           /* reserved (non-Lamport flag; unused on one GPU) */
     uint32_t lamport_flag;   /* current slot = lamport_flag % 3 */
-    uint32_t pad0;
+    uint32_t clear_elem_bytes; /* bytes per element of clear_size: the element size of
+                                  the call that filled the retired slot (2 or 4) */
     uint64_t comm_size;      /* bytes of one Lamport slot */
     uint64_t clear_size;     /* elements of the retired slot still to be cleared */
     int32_t status;          /* AR_OK or the first device-side error (AR_ERR_TIMEOUT) */
@@ -420,11 +421,27 @@ int ar_fusion_sum_ex(const void* const* bufs, int nranks, size_t n, int dtype, i
  * Sharing: every call on a device uses the same array and leaves the slot
  * state for the next call; calls whose work overlaps on the GPU (different
  * streams without ordering between them) race on it and give undefined
- * results.  Serialise them (one stream, or events). */
+ * results.  Serialise them (one stream, or events).  Consecutive calls may
+ * change element type, ranks and sizes: each call clears exactly the bytes
+ * its predecessor left in the retired slot.
+ * Device-side errors: a bounded wait that gives up (only possible when calls
+ * overlap) records AR_ERR_TIMEOUT in the array's status word, which later
+ * calls do not erase; read it with ar_fusion_noalloc_status. */
 int ar_fusion_run_noalloc(const void* const* partials, int nranks, int tokens, int hidden_dim,
                           int dtype, const void* residual_in, const void* gamma, float eps,
                           int pattern, void* residual_out, void* norm_out, void* quant_out,
                           void* scale_out, const float* scale_factor, void* stream);
+
+/* Device-side status of ar_fusion_run_noalloc on the current device (no
+ * counterpart on the pages).  Synchronises `stream`, then returns the first
+ * device-side error recorded by a no-allocation call since set-up or since
+ * the previous ar_fusion_noalloc_status call (AR_OK if none; AR_ERR_TIMEOUT
+ * when a wait gave up, outputs of that call undefined) and clears it.
+ * *detail (may be NULL) receives where it happened -- row * 32 + rank for a
+ * wait on a rank's data -- or -1.  Before the first no-allocation call on the
+ * device it returns AR_OK and touches nothing.  Allocates nothing; returns
+ * AR_ERR_CUDA if reading the status word fails. */
+int ar_fusion_noalloc_status(void* stream, int* detail);
 
 /* ---------------------------------------------------------- utilities -- */
 
