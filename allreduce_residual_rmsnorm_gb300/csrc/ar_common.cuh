@@ -496,19 +496,6 @@ __host__ __device__ __forceinline__ void two_sum(float a, float b, float& s, flo
     err = rn_add(rn_add(a, -rn_add(s, -bb)), rn_add(b, -bb));
 }
 
-// a += t for a non-negative running sum and term (sums of squares): ordering
-// the two by max / min makes Dekker's fast two-sum exact (one operation fewer
-// than TwoSum); the new high part is hi + t itself, so a NaN term propagates.
-__host__ __device__ __forceinline__ void df_add_nonneg(DF& a, float t)
-{
-    const float s = rn_add(a.hi, t);
-    const float big = fmaxf(a.hi, t);
-    const float small = fminf(a.hi, t);
-    const float err = rn_add(rn_add(big, -s), small);
-    a.hi = s;
-    a.lo = rn_add(a.lo, err);
-}
-
 // Pair addition: the high parts are added exactly (TwoSum) and every rounding
 // error lands in lo; lo is not renormalised into hi between steps (its own
 // rounding errors are ~2^-24 of an already tiny value), which keeps the
@@ -524,6 +511,66 @@ __host__ __device__ __forceinline__ DF df_add(DF a, DF b)
 __host__ __device__ __forceinline__ float df_round(DF a)
 {
     return rn_add(a.hi, a.lo);
+}
+
+// ------------------------------------------------------- packed fp32 pairs
+//
+// Two fp32 values handled by one packed instruction on the device
+// (add / sub / mul .rn.f32x2: each lane rounded to nearest exactly as the
+// scalar instruction, subnormals kept); the host form does the same per lane.
+
+struct F2 {
+    float x, y;
+};
+
+#ifdef __CUDA_ARCH__
+#define AR_F2_OP(name, op)                                                              \
+    __host__ __device__ __forceinline__ F2 name(F2 a, F2 b)                             \
+    {                                                                                   \
+        F2 r;                                                                           \
+        asm("{\n\t.reg .b64 pa, pb, pr;\n\tmov.b64 pa, {%2, %3};\n\t"                     \
+            "mov.b64 pb, {%4, %5};\n\t" op " pr, pa, pb;\n\tmov.b64 {%0, %1}, pr;\n\t}"    \
+            : "=f"(r.x), "=f"(r.y)                                                      \
+            : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));                                  \
+        return r;                                                                       \
+    }
+#else
+#define AR_F2_OP(name, op)                                                              \
+    __host__ __device__ __forceinline__ F2 name(F2 a, F2 b)                             \
+    {                                                                                   \
+        return F2{name##_1(a.x, b.x), name##_1(a.y, b.y)};                              \
+    }
+__host__ __device__ __forceinline__ float f2_add_1(float a, float b) { return a + b; }
+__host__ __device__ __forceinline__ float f2_sub_1(float a, float b) { return a - b; }
+__host__ __device__ __forceinline__ float f2_mul_1(float a, float b) { return a * b; }
+#endif
+AR_F2_OP(f2_add, "add.rn.f32x2")
+AR_F2_OP(f2_sub, "sub.rn.f32x2")
+AR_F2_OP(f2_mul, "mul.rn.f32x2")
+#undef AR_F2_OP
+
+// Two double-float accumulators side by side (lane 0: even elements, lane 1:
+// odd elements), updated by one TwoSum per lane in packed instructions:
+// hi + lo keeps the exact sum of the terms up to the rounding of lo, as DF.
+struct DF2 {
+    F2 hi, lo;
+};
+
+// a += t per lane (TwoSum on the high parts, its error into lo; exact for
+// any two finite terms, no ordering needed)
+__host__ __device__ __forceinline__ void df2_add_terms(DF2& a, F2 t)
+{
+    const F2 s = f2_add(a.hi, t);
+    const F2 bb = f2_sub(s, a.hi);
+    const F2 err = f2_add(f2_sub(a.hi, f2_sub(s, bb)), f2_sub(t, bb));
+    a.hi = s;
+    a.lo = f2_add(a.lo, err);
+}
+
+// the two lanes as one pair (a TwoSum of the high parts, as df_add)
+__host__ __device__ __forceinline__ DF df2_merge(const DF2& a)
+{
+    return df_add(DF{a.hi.x, a.lo.x}, DF{a.hi.y, a.lo.y});
 }
 
 __device__ __forceinline__ DF df_shfl_xor(DF a, int m)

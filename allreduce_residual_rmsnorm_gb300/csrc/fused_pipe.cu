@@ -261,7 +261,7 @@ fused_pipe_kernel(const FusedArgs a, const int S, const int NC)
     int parity = 0;
     for (int row = blockIdx.x; row < a.T; row += gridDim.x) {
         const size_t roff = (size_t)row * row_bytes;
-        DF ss = {0.0f, 0.0f};
+        DF2 ss = {};
         V yv[VPT];
         bool ok = true;
 #pragma unroll
@@ -322,7 +322,7 @@ fused_pipe_kernel(const FusedArgs a, const int S, const int NC)
             }
         }
         bool stop = false;
-        const float rstd = consumer_row_rstd(ss, red + parity * 32, &rstd_sh[parity],
+        const float rstd = consumer_row_rstd(df2_merge(ss), red + parity * 32, &rstd_sh[parity],
                                              &stop_sh[parity], abort_flag, warp, lane, ncw, H,
                                              a.eps, NamedSync{NC}, stop);
         parity ^= 1;

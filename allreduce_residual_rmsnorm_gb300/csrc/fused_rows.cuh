@@ -26,6 +26,7 @@
 
 #include "fused_core.cuh"
 
+
 namespace arf {
 
 // Threads of a one-vector-per-thread row block (one_vec_threads_for).
@@ -176,9 +177,39 @@ fused_rows_kernel(const FusedArgs a)
     int parity = 0;
     float amax_local = 0.0f;
 
+    // One vector per thread, one row per block, at most 4 ranks: the next
+    // row's rank vectors and residual vector are loaded into registers as soon
+    // as this row's sum is formed, so those loads are in flight through this
+    // row's reduction barriers, normalisation and stores.  Measured (us,
+    // back-to-back / inputs evicted): R=4, T=2048, H=8192 with FP8 output
+    // 45.4 / 54.4 -> 39.9 / 50.3; R=4, T=8192, H=7168 128.7 / 140.1 ->
+    // 120.3 / 131.2.  With 8 or 16 ranks the 896-thread blocks have registers
+    // for two ranks ahead only, which measured slower (R=8, H=7168: 180 ->
+    // 221 us), so those rows load as before.
+    constexpr bool PIPE = !WARP_ROW && !CLUSTER && VPT == 1 && RMAX <= 4;
+    V pre[KCH][RB];
+    V pre_x[KCH];
+    const auto load_first = [&](int r_) {
+#pragma unroll
+        for (int kk = 0; kk < KCH; ++kk) {
+            const int v = g + kk * G;
+            if (v < Hv) {
+                const size_t o = (size_t)r_ * H * EB + (size_t)v * VB;
+#pragma unroll
+                for (int rr = 0; rr < RB; ++rr)
+                    if (rr < R)
+                        pre[kk][rr] = a.lamport ? ld_poll_v<D>(AR_RANK_PTR(rr) + o)
+                                                : ld_stream_v<D>(AR_RANK_PTR(rr) + o);
+                pre_x[kk] = ld_stream_v<D>(a.residual_in + o);
+            }
+        }
+    };
+    if (PIPE && row < a.T)
+        load_first(row);
+
     for (; row < a.T; row += row_step) {
         const size_t roff = (size_t)row * H * EB;
-        DF ss = {0.0f, 0.0f};
+        DF2 ss = {};
         V yv[VPT];
 
         // One-row-per-block, staged or caller partials: while this row is
@@ -213,7 +244,12 @@ fused_rows_kernel(const FusedArgs a)
 #pragma unroll
                 for (int kk = 0; kk < KCH; ++kk) {
                     const int v = g + (k0 + kk) * G;
-                    if (v < Hv) {
+                    if (PIPE && r0 == 0) {
+#pragma unroll
+                        for (int rr = 0; rr < RB; ++rr)
+                            raw[kk][rr] = pre[kk][rr];
+                        xr[kk] = pre_x[kk];
+                    } else if (v < Hv) {
 #pragma unroll
                         for (int rr = 0; rr < RB; ++rr)
                             if (r0 + rr < R)
@@ -285,13 +321,16 @@ fused_rows_kernel(const FusedArgs a)
                 }
             }
         }
+        if (PIPE && row + row_step < a.T)
+            load_first(row + row_step);
 
         // ---- sum of squares over the row
         float rstd;
+        const DF ssm = df2_merge(ss);
         if (WARP_ROW) {
-            rstd = inv_rms(df_warp_sum(ss), H, a.eps);
+            rstd = inv_rms(df_warp_sum(ssm), H, a.eps);
         } else if (!CLUSTER) {
-            rstd = row_rstd(ss, red[parity], &rstd_sh[parity], warp, lane, nwarps, H, a.eps,
+            rstd = row_rstd(ssm, red[parity], &rstd_sh[parity], warp, lane, nwarps, H, a.eps,
                             BlockSync{});
             parity ^= 1;
         } else {
@@ -300,9 +339,9 @@ fused_rows_kernel(const FusedArgs a)
             // shared memory.  Partials alternate by row parity, so one cluster
             // barrier per row suffices (a CTA can only overwrite part[p] two
             // rows later, after every CTA has passed the next barrier).
-            ss = df_warp_sum(ss);
+            const DF sw = df_warp_sum(ssm);
             if (lane == 0)
-                red[parity][warp] = ss;
+                red[parity][warp] = sw;
             __syncthreads();
             if (warp == 0) {
                 DF v = lane < nwarps ? red[parity][lane] : DF{0.0f, 0.0f};

@@ -1,8 +1,12 @@
 // Host-side check of the double-float sum-of-squares helpers of
-// ar_common.cuh (the same source the kernels use, compiled for the CPU):
-// per-thread accumulation (the fast two-sum for non-negative terms) followed
-// by a butterfly of df_add, as in a warp reduction, must give the exact sum
-// of squares rounded once to fp32, with every lane ending on the same bits.
+// ar_common.cuh (the same source the kernels use, compiled for the CPU; the
+// packed pair operations run per lane):
+// per-thread accumulation (two lanes, even and odd terms, each by TwoSum),
+// the merge of the two lanes, then a butterfly of df_add as in a warp
+// reduction must give the exact sum of squares rounded once to fp32, with
+// every lane of the butterfly ending on the same bits.
+// Built with -DAR_DF_CHECK_PLANT=1 the accumulation drops the TwoSum errors
+// (a plain fp32 sum of the terms): that build must fail the check.
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -10,7 +14,13 @@
 
 #include "ar_common.cuh"
 
+#ifndef AR_DF_CHECK_PLANT
+#define AR_DF_CHECK_PLANT 0
+#endif
+
 using arf::DF;
+using arf::DF2;
+using arf::F2;
 
 static float bf16_trunc(float x)
 {
@@ -27,20 +37,26 @@ int main()
     std::uniform_real_distribution<float> mag(-8.0f, 8.0f);
     std::uniform_int_distribution<int> sign(0, 1);
     int bad = 0, total = 0;
+    const auto draw = [&]() {
+        float y = bf16_trunc(ldexpf(1.0f + (mag(rng) + 8.0f) / 16.0f, (int)mag(rng)));
+        return sign(rng) ? -y : y;
+    };
     for (int trial = 0; trial < 800; ++trial) {
         const int lanes = 32, per = 8 * (1 + (trial / 2) % 32);  // up to 8192 terms per row
         DF acc[32];
         long double exact = 0.0L;
         for (int l = 0; l < lanes; ++l) {
-            acc[l] = DF{0.0f, 0.0f};
-            for (int i = 0; i < per; ++i) {
-                float y = bf16_trunc(ldexpf(1.0f + (mag(rng) + 8.0f) / 16.0f, (int)mag(rng)));
-                if (sign(rng))
-                    y = -y;
-                const float t = y * y;                       // exact: 8-bit significand
-                exact += (long double)t;
-                arf::df_add_nonneg(acc[l], t);
+            DF2 a2 = {};
+            for (int i = 0; i < per; i += 2) {
+                const float y0 = draw(), y1 = draw();
+                const F2 t = {y0 * y0, y1 * y1};             // exact: 8-bit significands
+                exact += (long double)t.x + (long double)t.y;
+                if (AR_DF_CHECK_PLANT)
+                    a2.hi = arf::f2_add(a2.hi, t);
+                else
+                    arf::df2_add_terms(a2, t);
             }
+            acc[l] = arf::df2_merge(a2);
         }
         for (int m = 16; m >= 1; m >>= 1) {                  // xor butterfly
             DF nxt[32];
@@ -56,7 +72,8 @@ int main()
         ++total;
         if (got != want) {
             ++bad;
-            printf("trial %d: got %.9g want %.9g\n", trial, got, want);
+            if (!AR_DF_CHECK_PLANT)
+                printf("trial %d: got %.9g want %.9g\n", trial, got, want);
         }
     }
     printf("%d/%d bad\n", bad, total);

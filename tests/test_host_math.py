@@ -7,12 +7,25 @@ from allreduce_residual_rmsnorm_gb300 import build as BUILD
 HERE = os.path.dirname(os.path.abspath(__file__))
 
 
-def test_double_float_sum_of_squares_is_correctly_rounded(tmp_path):
-    exe = tmp_path / "df_check"
+def _df_check(tmp_path, plant: int):
+    exe = tmp_path / f"df_check_{plant}"
     subprocess.check_call([BUILD.nvcc(), "-O2", "-std=c++17", "-I", BUILD.INCLUDE, "-I", BUILD.CSRC,
+                           f"-DAR_DF_CHECK_PLANT={plant}",
                            os.path.join(HERE, "host_df_check.cu"), "-o", str(exe)])
-    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    return subprocess.run([str(exe)], capture_output=True, text=True)
+
+
+def test_double_float_sum_of_squares_is_correctly_rounded(tmp_path):
+    r = _df_check(tmp_path, 0)
     assert r.returncode == 0, r.stdout + r.stderr
+
+
+def test_double_float_check_rejects_a_plain_fp32_sum(tmp_path):
+    """The same check with the TwoSum errors dropped must fail most trials."""
+    r = _df_check(tmp_path, 1)
+    assert r.returncode != 0
+    bad = int(r.stdout.strip().split()[0].split("/")[0])
+    assert bad > 400, r.stdout
 
 
 # ---- the packed 16-bit residual add: rnd16(fp32(a + b)) == rnd16(a + b)

@@ -342,6 +342,41 @@ def test_lamport_wait_times_out_and_reset_recovers():
     B.ar_fusion_workspace_destroy(ws)
 
 
+def test_bulk_pipe_with_a_1ns_wait_bound_is_correct_or_reports_a_timeout():
+    """The bulk-copy pipe with a 1 ns bound per stage wait.  Each wait first
+    suspends in the barrier unit until its phase completes, so in practice no
+    wait runs out; whichever happens, a call must either finish with the
+    oracle's outputs and a clean status, or report AR_ERR_TIMEOUT from a
+    consumer (-1) or producer (-2) wait and end (every copy it issued lands
+    before its block exits: the producer's final wait for its copies keeps a
+    floor of 200 ms).  After a reset, with the default bound, the workspace
+    computes the oracle's outputs."""
+    w = W.FusedWorkload("pipe_tiny_bound", R=8, T=304, H=16384, pattern=W.RES_NORM)
+    inp = W.make_fused_inputs(w)
+    exp = PY.oracle_expected(w, inp)
+    ws = make_ws(w)
+    B.ar_fusion_workspace_set_variant(ws, B.AR_VARIANT_BULK_PIPE)
+    B.ar_fusion_workspace_set_timeout_ns(ws, 1)
+    outcomes = []
+    for _ in range(5):
+        got = PY.run_gpu(ws, w, inp)
+        assert B.ar_fusion_workspace_info(ws)["last_variant"] == B.AR_VARIANT_BULK_PIPE
+        rc, detail = B.ar_fusion_workspace_status(ws)
+        if rc == 0:
+            PY.check_all(w, got, exp)
+        else:
+            assert rc == B.AR_ERR_TIMEOUT and detail in (-1, -2), (rc, detail)
+            B.ar_fusion_workspace_reset(ws)
+        outcomes.append(rc)
+    B.ar_fusion_workspace_reset(ws)
+    assert B.ar_fusion_workspace_status(ws)[0] == 0
+    B.ar_fusion_workspace_set_timeout_ns(ws, 2_000_000_000)
+    got = PY.run_gpu(ws, w, inp)
+    PY.check_all(w, got, exp)
+    assert B.ar_fusion_workspace_status(ws)[0] == 0
+    B.ar_fusion_workspace_destroy(ws)
+
+
 # --------------------------------------------------------------- ABI errors
 
 def test_abi_errors_launch_nothing():
