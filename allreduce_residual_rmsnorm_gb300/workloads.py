@@ -118,13 +118,18 @@ def make_fused_inputs(w: FusedWorkload) -> FusedInputs:
     return FusedInputs(partials, residual, gamma, w.eps)
 
 
-def make_sum_inputs(w: SumWorkload) -> torch.Tensor:
-    g = torch.Generator(device="cpu")
+def make_sum_inputs(w: SumWorkload, device: str = "cpu") -> torch.Tensor:
+    """[R, N] inputs, each rank (rand(N) * 2 - 1) -> D.  ``device`` picks where
+    the seeded generator runs: the CPU stream (default, what parity tests
+    use) or a device generator (same recipe and distribution, another stream;
+    for inputs too large to draw on the host quickly)."""
+    g = torch.Generator(device=device)
     g.manual_seed(w.seed)
     dt = torch_dtype(w.dtype)
-    out = torch.empty((w.R, w.N), dtype=dt)
+    out = torch.empty((w.R, w.N), dtype=dt, device=device)
     for r in range(w.R):
-        out[r].copy_(torch.rand((w.N,), generator=g, dtype=torch.float32).mul_(2.0).sub_(1.0))
+        out[r].copy_(torch.rand((w.N,), generator=g, dtype=torch.float32, device=device)
+                     .mul_(2.0).sub_(1.0))
     return out
 
 
