@@ -405,9 +405,9 @@ def run_sweep(args):
 
         # launch options: (cluster CTAs per row, programmatic dependent launch);
         # decode-sized token counts also try cluster-split rows and PDL
-        opts = [(0, 0)]
+        opts = [(0, 1)]
         if w.T < 152 and w.H > 1024:
-            opts += [(1, 1), (2, 0), (2, 1), (4, 1), (8, 1)]
+            opts += [(1, 0), (2, 1), (4, 1), (8, 1)]
         for cl, pdl in opts:
             B.ar_fusion_workspace_set_launch(ws, cl, pdl)
             if not lam:
@@ -420,7 +420,7 @@ def run_sweep(args):
         if w is W.NVFP4_PREFILL:
             # the precision and layout options on the benchmarked workload:
             # element-type accumulation, NVFP4 scales in the 128 x 4 tile layout
-            B.ar_fusion_workspace_set_launch(ws, 0, 0)
+            B.ar_fusion_workspace_set_launch(ws, 0, 1)
             sf_swz = torch.zeros(B.swizzled_scale_bytes(w.T, w.H), dtype=torch.uint8, device=dev)
             for opt in ("acc_element", "sf_swizzled"):
                 B.ar_fusion_workspace_set_accumulate(
@@ -442,7 +442,7 @@ def run_sweep(args):
         eb = 4 if w.dtype == "fp32" else 2
         if (w.R + 3) * w.T * w.H * eb < 2 * l2_bytes:
             # caller partials (no staging), inputs evicted before every call
-            B.ar_fusion_workspace_set_launch(ws, 0, 0)
+            B.ar_fusion_workspace_set_launch(ws, 0, 1)
             parts = [P[r] for r in range(w.R)]
             us = cold_us(lambda: B.ar_fusion_run(ws, parts, X, G, w.eps, pat, out["res"],
                                                  out["norm"], q, sf, sc))
@@ -550,7 +550,7 @@ def quant_scale(pat, amax, B):
     return np.float32(2688.0) / a
 
 
-def run_configs(timer, peak, dev, B, W):
+def run_configs(timer, peak, dev, B, W, clocks=None):
     """The five target workloads, one call each under the same conditions as
     --sweep (CUDA graphs; Lamport workloads timed as stage + call minus
     stage, inputs L2-resident; working sets below 2 x L2 also cold, caller
@@ -588,9 +588,29 @@ def run_configs(timer, peak, dev, B, W):
         e = {"workload": w.name, "R": w.R, "T": w.T, "H": w.H, "dtype": w.dtype,
              "pattern": w.pattern, "mode": "lamport" if lam else "buffer"}
         byts = fused_alg_bytes(w, pat, B)
+        t0 = time.time()
         if lam:
-            us = timer.warm(lambda: (stage(), call())) - timer.warm(stage)
+            st_us = timer.warm(stage)
+            both_us = timer.warm(lambda: (stage(), call()))
+            us = both_us - st_us
             e["l2"] = "staged inputs L2-resident (stage + call minus stage)"
+            # the parts of that difference, and the same call in buffer mode on
+            # caller partials (no sentinel poll or clear), for comparison
+            def stage_buf():
+                for r in range(w.R):
+                    B.ar_fusion_workspace_stage(ws, r, P[r], mode=B.AR_MODE_BUFFER)
+
+            def call_buf():
+                B.ar_fusion_workspace_set_mode(ws, B.AR_MODE_BUFFER)
+                B.ar_fusion_run(ws, None, X, G, w.eps, pat, res, nrm, q, None, sc)
+                B.ar_fusion_workspace_set_mode(ws, B.AR_MODE_AUTO)
+
+            e["lamport_parts"] = {
+                "stage_us": st_us, "stage_and_call_us": both_us,
+                "caller_partials_us": timer.warm(lambda: B.ar_fusion_run(
+                    ws, parts, X, G, w.eps, pat, res, nrm, q, None, sc)),
+                "buffer_staged_us": timer.warm(lambda: (stage_buf(), call_buf()))
+                - timer.warm(stage_buf)}
         else:
             stage()
             us = timer.warm(call)
@@ -604,6 +624,10 @@ def run_configs(timer, peak, dev, B, W):
                          "gbs": byts / (uc * 1e-6) / 1e9, "frac": byts / (uc * 1e-6) / 1e9 / peak,
                          "l2": f"caller partials, {3 * timer.l2_bytes / 1e6:.0f} MB read "
                                "before every call"}
+        if clocks is not None:
+            ck = clocks.summary(t0, time.time())
+            e["clocks"] = {"sm_mhz": ck.get("sm_mhz"), "samples": ck.get("samples"),
+                           "reasons": ck.get("reasons")}
         # one more call on fresh outputs, in the mode timed, for the parity check
         res.fill_(float("nan"))
         nrm.fill_(float("nan"))
@@ -977,7 +1001,7 @@ def main():
     t_cfg0 = time.time()
     if not args.profile and not args.no_configs and world == 1:
         timer = GraphTimer(dev, args.warmup)
-        entries, outputs = run_configs(timer, peak, dev, B, W)
+        entries, outputs = run_configs(timer, peak, dev, B, W, clocks)
         # (a call on the current stream, so that graph capture records it)
         hl_us = timer.warm(lambda: B.ar_fusion_run(ws, None, X, G, w.eps, pattern,
                                                    residual_out=res, quant_out=q, scale_out=sf,

@@ -266,10 +266,13 @@ int ar_fusion_workspace_set_mode(ar_fusion_ws* ws, int mode);
  * row: the split measured slower wherever the library picks the row
  * kernel), 1 = no cluster, 2, 4 or 8;
  * used only where each CTA of the cluster still holds one vector (8
- * elements) per thread.  pdl: 1 = programmatic dependent launch (the same
- * launcher's programmaticStreamSerialization attribute): the fused kernel
- * may be scheduled while the preceding kernel on the stream finishes and
- * waits on the device for its results.  Errors: AR_ERR_INVALID. */
+ * elements) per thread.  pdl: 1 (the default) = programmatic dependent
+ * launch (the same launcher's programmaticStreamSerialization attribute):
+ * the fused kernel may be scheduled while the preceding kernel on the
+ * stream finishes and waits on the device for its results before its first
+ * read, which is safe after any kernel; 0 = plain stream order.  The
+ * bulk-copy pipe always launches in plain stream order.  Errors:
+ * AR_ERR_INVALID. */
 int ar_fusion_workspace_set_launch(ar_fusion_ws* ws, int cluster_size, int pdl);
 
 /* Accumulation of the rank sum of later fused calls (enum ar_accumulate;

@@ -2,8 +2,12 @@
 and through the CPU oracle, and compare under the stated tolerances.
 
 Tolerances (per element): |g - o| <= atol + rtol * |o| with (2e-2, 1e-2) for
-bf16, (5e-3, 5e-3) for fp16 and (1e-5, 1e-5) for fp32.  Quantised codes must
-be bit-exact except that at most 0.1% may differ by one code step.
+bf16, (5e-3, 5e-3) for fp16 and (1e-5, 1e-5) for fp32.  The same two numbers
+also bound, separately, the maximum absolute error and the maximum relative
+error of each output (the relative one over expected values in the normal
+range of the element type: a subnormal value's last bit is a large fraction
+of it).  Quantised codes must be bit-exact except that at most 0.1% may
+differ by one code step.
 """
 from __future__ import annotations
 
@@ -105,7 +109,22 @@ def run_gpu(ws, w: W.FusedWorkload, inp: W.FusedInputs, scale: float | None = No
     return out
 
 
-def assert_close16(got_bits, exp_bits, dtype: str, what: str, require_exact_frac: float = 0.0):
+MIN_NORMAL = {"bf16": 2.0 ** -126, "fp16": 2.0 ** -14, "fp32": 2.0 ** -126}
+
+
+def error_stats(got_bits, exp_bits, dtype: str):
+    """(max abs error, max rel error over normal-range expected values)."""
+    g = to_float(got_bits, dtype).astype(np.float64)
+    o = to_float(exp_bits, dtype).astype(np.float64)
+    err = np.abs(g - o)
+    err[np.isnan(g) & np.isnan(o)] = 0.0
+    nrm = np.abs(o) >= MIN_NORMAL[dtype]
+    rel = err[nrm] / np.abs(o[nrm])
+    return float(np.max(err, initial=0.0)), float(np.max(rel, initial=0.0))
+
+
+def assert_close16(got_bits, exp_bits, dtype: str, what: str, require_exact_frac: float = 0.0,
+                   errors: dict | None = None):
     atol, rtol = TOL[dtype]
     g = to_float(got_bits, dtype)
     o = to_float(exp_bits, dtype)
@@ -113,6 +132,11 @@ def assert_close16(got_bits, exp_bits, dtype: str, what: str, require_exact_frac
     bad = ~(err <= atol + rtol * np.abs(o))
     assert not bad.any(), (f"{what}: {bad.sum()} elements outside tolerance; max abs err "
                            f"{np.nanmax(err)} at {np.argwhere(bad)[:5].tolist()}")
+    max_abs, max_rel = error_stats(got_bits, exp_bits, dtype)
+    assert max_abs <= atol, f"{what}: max abs error {max_abs} > {atol}"
+    assert max_rel <= rtol, f"{what}: max rel error {max_rel} > {rtol}"
+    if errors is not None:
+        errors[what] = {"max_abs_err": max_abs, "max_rel_err": max_rel}
     mism = np.count_nonzero(got_bits != exp_bits)
     return mism
 
@@ -148,12 +172,15 @@ def assert_codes(got: np.ndarray, exp: np.ndarray, kind: str, what: str):
 def check_all(w: W.FusedWorkload, got: dict, exp: dict):
     """Apply every rule; returns a dict of mismatch counts (for reporting)."""
     stats = {}
+    errs = {}
     pat = B.PATTERNS[w.pattern]
     if pat & B.AR_RESIDUAL_OUT:
         stats["residual_mismatch"] = assert_close16(got["residual"], exp["residual"], w.dtype,
-                                                    "residual_out")
+                                                    "residual_out", errors=errs)
     if pat & B.AR_NORM_OUT:
-        stats["norm_mismatch"] = assert_close16(got["norm"], exp["norm"], w.dtype, "norm_out")
+        stats["norm_mismatch"] = assert_close16(got["norm"], exp["norm"], w.dtype, "norm_out",
+                                                errors=errs)
+    stats["errors"] = errs
     if pat & B.AR_QUANT_FP8:
         stats["fp8_off"] = assert_codes(got["quant"], exp["quant"], "e4m3", "fp8 codes")
     if pat & B.AR_QUANT_NVFP4:

@@ -22,7 +22,7 @@ def make_ws(w, max_tokens=None, mem=False):
 
 
 def run_and_check(w, variant=B.AR_VARIANT_AUTO, staged=False, mode=B.AR_MODE_AUTO, inp=None,
-                  max_tokens=None, cluster=0, pdl=0, acc=B.AR_ACC_FP32):
+                  max_tokens=None, cluster=0, pdl=1, acc=B.AR_ACC_FP32):
     inp = inp or W.make_fused_inputs(w)
     ws = make_ws(w, max_tokens)
     B.ar_fusion_workspace_set_variant(ws, variant)
@@ -46,18 +46,21 @@ def run_and_check(w, variant=B.AR_VARIANT_AUTO, staged=False, mode=B.AR_MODE_AUT
 @pytest.mark.parametrize("staged", [False, True])
 def test_tiny_r2_t16_h512(variant, staged):
     stats, _, _ = run_and_check(W.TINY, variant, staged)
+    print(W.TINY.name, stats)
     assert stats["residual_mismatch"] == 0 and stats["norm_mismatch"] == 0, stats
 
 
 @pytest.mark.parametrize("staged", [False, True])
 def test_decode_r8_t128_h4096(staged):
     stats, _, _ = run_and_check(W.DECODE, B.AR_VARIANT_AUTO, staged)
+    print(W.DECODE.name, stats)
     assert stats["residual_mismatch"] == 0 and stats["norm_mismatch"] == 0, stats
 
 
 @pytest.mark.parametrize("variant", [B.AR_VARIANT_AUTO, B.AR_VARIANT_CTA_ROW, B.AR_VARIANT_BULK_PIPE])
 def test_fp8_r4_t2048_h8192(variant):
     stats, _, _ = run_and_check(W.FP8_PREFILL, variant, staged=True)
+    print(W.FP8_PREFILL.name, stats)
     assert stats["residual_mismatch"] == 0, stats
     assert stats["norm_mismatch"] <= 0.00001 * W.FP8_PREFILL.T * W.FP8_PREFILL.H, stats
 
@@ -67,6 +70,7 @@ def test_fp8_r4_t2048_h8192(variant):
 def test_nvfp4_r8_t8192_h7168_full_size(variant, staged):
     # the benchmarked configuration, element by element over every output
     stats, _, _ = run_and_check(W.NVFP4_PREFILL, variant, staged)
+    print(W.NVFP4_PREFILL.name, stats)
     assert stats["residual_mismatch"] == 0, stats
 
 

@@ -23,7 +23,9 @@ def test_oracle_outputs_pass_with_no_mismatch(dtype):
     for pattern in (W.RES_NORM, W.RES_NORM_FP8, W.RES_NORM_NVFP4):
         w, exp, got = expected(pattern, dtype)
         stats = PY.check_all(w, got, exp)
-        assert all(v == 0 for v in stats.values()), stats
+        assert all(v == 0 for k, v in stats.items() if k != "errors"), stats
+        assert all(e["max_abs_err"] == 0.0 and e["max_rel_err"] == 0.0
+                   for e in stats["errors"].values()), stats
 
 
 def test_one_residual_bit_is_counted():
