@@ -44,15 +44,15 @@ constexpr int rows_max_threads()
     return WARP_ROW ? 256 : (VPT == 1 ? one_vec_threads<D>(RMAX) : 512);
 }
 
-// Two rows per SM: 16-bit rows of 513..1024 vectors with at most 4 ranks run
-// as blocks of <= 512 threads at two vectors per thread and one vector per
-// load batch, within 64 registers, so that two blocks (two rows) share an SM
-// and one row's reductions overlap the other's loads (the launcher picks this
-// for light rows, see launch_fused_rows_t).
-template <class D, int RMAX, int VPT, bool WARP_ROW>
+// LIGHT, two rows per SM: 16-bit rows of 513..1024 vectors with at most 4
+// ranks run as blocks of <= 512 threads at two vectors per thread and one
+// vector per load batch, within 64 registers, so that two blocks (two rows)
+// share an SM and one row's reductions overlap the other's loads (the
+// launcher picks this for light rows, see launch_fused_rows_t).
+template <bool LIGHT>
 __host__ __device__ constexpr int rows_min_blocks()
 {
-    return (!WARP_ROW && D::bytes == 2 && VPT == 2 && RMAX <= 4) ? 2 : 1;
+    return LIGHT ? 2 : 1;
 }
 
 // s[kk] (+)= rank batch r0..r0+RB-1 of vector g + (k0 + kk) * G; ELEM rounds
@@ -88,9 +88,9 @@ __device__ __forceinline__ void fold_ranks(float (&s)[KCH][8],
 // CLUSTER: the kernel is launched with a thread-block cluster and one row
 // spans its CTAs (a separate instantiation, so the common one-CTA-per-row
 // kernel carries none of the cluster code).
-template <class D, int RMAX, int VPT, bool WARP_ROW, bool CLUSTER = false>
+template <class D, int RMAX, int VPT, bool WARP_ROW, bool CLUSTER = false, bool LIGHT = false>
 __global__ void __launch_bounds__(rows_max_threads<D, RMAX, VPT, WARP_ROW>(),
-                                  rows_min_blocks<D, RMAX, VPT, WARP_ROW>())
+                                  rows_min_blocks<LIGHT>())
 fused_rows_kernel(const FusedArgs a)
 {
     using V = typename D::Vec;
@@ -106,9 +106,9 @@ fused_rows_kernel(const FusedArgs a)
     constexpr int RBMAX = 8;
     constexpr int RB = RMAX < RBMAX ? RMAX : RBMAX;
     // vectors per batch (one in the two-rows-per-SM form)
-    constexpr int KCH = rows_min_blocks<D, RMAX, VPT, WARP_ROW>() == 2
-                            ? 1
-                            : ((LOADS / RB) > VPT ? VPT : (LOADS / RB));
+    constexpr int KCH = LIGHT ? 1 : ((LOADS / RB) > VPT ? VPT : (LOADS / RB));
+    static_assert(!LIGHT || (D::bytes == 2 && VPT == 2 && RMAX <= 4 && !WARP_ROW && !CLUSTER),
+                  "two rows per SM: 16-bit, two vectors per thread, at most 4 ranks");
     static_assert(VPT % KCH == 0, "batch must divide VPT");
     static_assert(RMAX % RB == 0, "rank batch must divide RMAX");
 
@@ -185,7 +185,9 @@ fused_rows_kernel(const FusedArgs a)
     // 45.4 / 54.4 -> 39.9 / 50.3; R=4, T=8192, H=7168 128.7 / 140.1 ->
     // 120.3 / 131.2.  With 8 or 16 ranks the 896-thread blocks have registers
     // for two ranks ahead only, which measured slower (R=8, H=7168: 180 ->
-    // 221 us), so those rows load as before.
+    // 221 us), so those rows load as before; so did two vectors per thread
+    // at 512 threads with the same look-ahead (R=4, H=8192: 65.9 us).  The
+    // row then works on `pre` / `pre_x` in place (no register copies).
     constexpr bool PIPE = !WARP_ROW && !CLUSTER && VPT == 1 && RMAX <= 4;
     V pre[KCH][RB];
     V pre_x[KCH];
@@ -234,21 +236,22 @@ fused_rows_kernel(const FusedArgs a)
 #pragma unroll
         for (int k0 = 0; k0 < VPT; k0 += KCH) {
             float s[KCH][8];
-            V xr[KCH];
+            // with PIPE (one chunk, one rank batch) the row's vectors are
+            // already in `pre` / `pre_x`: work on them in place
+            V xr_own[KCH];
+            V (&xr)[KCH] = PIPE ? pre_x : xr_own;
 #pragma unroll
             for (int r0 = 0; r0 < RMAX; r0 += RB) {
                 if (r0 >= R)
                     break;
-                V raw[KCH][RB];
+                V raw_own[KCH][RB];
+                V (&raw)[KCH][RB] = PIPE ? pre : raw_own;
                 // ---- loads of this batch (all in flight together)
 #pragma unroll
                 for (int kk = 0; kk < KCH; ++kk) {
                     const int v = g + (k0 + kk) * G;
-                    if (PIPE && r0 == 0) {
-#pragma unroll
-                        for (int rr = 0; rr < RB; ++rr)
-                            raw[kk][rr] = pre[kk][rr];
-                        xr[kk] = pre_x[kk];
+                    if (PIPE) {
+                        // loaded by load_first
                     } else if (v < Hv) {
 #pragma unroll
                         for (int rr = 0; rr < RB; ++rr)

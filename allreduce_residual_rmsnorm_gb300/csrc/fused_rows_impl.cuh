@@ -32,6 +32,20 @@ static const void* rows_fn_vpt(int vpt)
     }
 }
 
+// two rows per SM (16-bit, at most 4 ranks, two vectors per thread)
+template <class D>
+static const void* rows_light_fn(int rmax)
+{
+    if constexpr (D::bytes == 2) {
+        switch (rmax) {
+        case 2: return (const void*)fused_rows_kernel<D, 2, 2, false, false, true>;
+        case 4: return (const void*)fused_rows_kernel<D, 4, 2, false, false, true>;
+        default: return nullptr;
+        }
+    }
+    return nullptr;
+}
+
 // one-vector-per-thread row kernels launched with a cluster
 template <class D>
 static const void* rows_cluster_fn(int rmax)
@@ -156,9 +170,12 @@ cudaError_t launch_fused_rows_t(int variant, const FusedArgs& a, const LaunchCfg
         // 95.1 / 108.2; R=4, H=6144: 111.2 / 116.8 vs 118.8 / 131.5.  Heavier
         // rows lose (R=4, H=8192, T=8192: 157.5 / 152.5 vs 143.2 / 154.4; at
         // T=2048 with FP8 output: 46.6 / 52.4 vs 45.3 / 54.5).
+        bool light = false;
         if (D::bytes == 2 && C == 1 && rmax <= 4 && Hv > 512 && Hv <= 1024 &&
-            a.R * Hv <= 3072 && a.T >= 2 * c.sms)
+            a.R * Hv <= 3072 && a.T >= 2 * c.sms) {
             vpt = 2;
+            light = true;
+        }
         // 1025..1536 vectors of a 16-bit row with at most 4 ranks: three
         // vectors per thread (up to 512 threads) instead of four (up to 384);
         // measured R=2, H=10240, T=16384: 256.4 vs 312.3 us; R=4, H=10240,
@@ -167,7 +184,8 @@ cudaError_t launch_fused_rows_t(int variant, const FusedArgs& a, const LaunchCfg
             vpt = 3;
         if (vpt > 8)
             return cudaErrorInvalidValue;
-        fn = (C > 1 && vpt == 1) ? rows_cluster_fn<D>(rmax) : rows_fn<D, false>(rmax, vpt);
+        fn = light ? rows_light_fn<D>(rmax)
+                   : (C > 1 && vpt == 1) ? rows_cluster_fn<D>(rmax) : rows_fn<D, false>(rmax, vpt);
         if (vpt != 1)
             C = 1;
         threads = ((Hv + C * vpt - 1) / (C * vpt) + 31) / 32 * 32;

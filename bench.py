@@ -75,7 +75,7 @@ def parse():
     c.add_argument("--pattern", default="res_nvfp4")
     c.add_argument("--dtype", default="bf16", choices=["bf16", "fp16", "fp32"])
     c.add_argument("--cluster", type=int, default=0)
-    c.add_argument("--pdl", type=int, default=0)
+    c.add_argument("--pdl", type=int, default=1)
     c.add_argument("--lamport", action="store_true")
     c.add_argument("--sum", type=int, default=0,
                    help="plain R-way fp16 sum of N elements per rank instead")
