@@ -5,8 +5,9 @@
 // Vector-aligned inputs (16 bytes; 32 for fp32): grid-stride over vectors of
 // 8 elements, two vectors per thread per step so 2R loads are in flight, and
 // the n % 8 tail elements done one by one (the page's vectorSum drops nothing
-// either: its 32-bit tail loop covers the rest).  Any misaligned pointer:
-// element-wise kernel.
+// either: its 32-bit tail loop covers the rest).  16-bit elements at any
+// element offset: aligned 16-byte loads realigned in registers.  Misaligned
+// fp32 pointers: element-wise kernel.
 #include <atomic>
 
 #include "ar_common.cuh"
@@ -131,6 +132,68 @@ __global__ void __launch_bounds__(256) vector_sum_kernel(const SumArgs a)
     }
 }
 
+// Bytes [m, m + 16) of the 32 bytes a:b (m even, 0..14): the 16-byte vector
+// that starts m bytes into the aligned block a.  m is the same for every
+// thread (one input's misalignment), so the selection does not diverge.
+__device__ __forceinline__ uint4 realign16(const uint4& a, const uint4& b, uint32_t m)
+{
+    uint32_t w0, w1, w2, w3, w4;
+    switch (m >> 2) {
+    case 0: w0 = a.x; w1 = a.y; w2 = a.z; w3 = a.w; w4 = b.x; break;
+    case 1: w0 = a.y; w1 = a.z; w2 = a.w; w3 = b.x; w4 = b.y; break;
+    case 2: w0 = a.z; w1 = a.w; w2 = b.x; w3 = b.y; w4 = b.z; break;
+    default: w0 = a.w; w1 = b.x; w2 = b.y; w3 = b.z; w4 = b.w; break;
+    }
+    const uint32_t sh = (m & 2u) * 8u;   // 0 or 16 bits: odd element offset
+    return make_uint4(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh),
+                      __funnelshift_r(w2, w3, sh), __funnelshift_r(w3, w4, sh));
+}
+
+// 16-bit elements, inputs or output not 16-byte aligned.  The output's
+// 16-byte grid, from its first aligned element h, defines vectors j of 8
+// elements; input r holds vector j at an address m_r bytes past a 16-byte
+// boundary (m_r the same for every j), read as the two aligned 16-byte
+// blocks that cover it and realigned in registers.  Vectors 1 .. nv-2 take
+// this path; their blocks lie inside the inputs (the block after vector j's
+// is inside vector j+1, the block before it inside vector j-1).  Elements
+// before vector 1 and from vector nv-1 on are summed one by one.
+template <class D, int RMAX>
+__global__ void __launch_bounds__(256) vector_sum_shift_kernel(const SumArgs a, const uint64_t h,
+                                                                const uint64_t nv)
+{
+    using V = typename D::Vec;
+    static_assert(D::bytes == 2, "16-bit elements");
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (uint64_t j = 1 + tid; j + 1 < nv; j += stride) {
+        const uint64_t off = 2 * (h + 8 * j);
+        V raw[RMAX];
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r) {
+            if (r < a.R) {
+                const uintptr_t p = (uintptr_t)a.in[r] + off;
+                const uint32_t m = (uint32_t)(p & 15u);
+                const uint4* blk = reinterpret_cast<const uint4*>(p - m);
+                const uint4 lo = __ldg(blk);
+                raw[r] = m ? realign16(lo, __ldg(blk + 1), m) : lo;
+            }
+        }
+        st_vec(a.out + off, sum_vec<D, RMAX>(a, raw));
+    }
+    // element by element: [0, h + 8) and [h + 8 * (nv - 1), n)
+    const uint64_t n_head = h + 8, tail0 = h + 8 * (nv - 1);
+    if (tid < n_head + (a.n - tail0)) {
+        const uint64_t e = tid < n_head ? tid : tail0 + (tid - n_head);
+        float s = ld_elem<D>(a.in[0], e);
+        for (int r = 1; r < a.R; ++r) {
+            s = __fadd_rn(s, ld_elem<D>(a.in[r], e));
+            if (a.acc)
+                s = round1<D>(s);
+        }
+        st_elem<D>(a.out, e, s);
+    }
+}
+
 template <class D>
 __global__ void __launch_bounds__(256) vector_sum_scalar_kernel(const SumArgs a)
 {
@@ -159,6 +222,21 @@ static const void* sum_fn(int rmax)
 }
 
 template <class D>
+static const void* shift_fn(int rmax)
+{
+    if constexpr (D::bytes == 2) {
+        switch (rmax) {
+        case 2: return (const void*)vector_sum_shift_kernel<D, 2>;
+        case 4: return (const void*)vector_sum_shift_kernel<D, 4>;
+        case 8: return (const void*)vector_sum_shift_kernel<D, 8>;
+        case 16: return (const void*)vector_sum_shift_kernel<D, 16>;
+        default: return nullptr;
+        }
+    }
+    return nullptr;
+}
+
+template <class D>
 static cudaError_t launch_t(const SumArgs& a, const LaunchCfg& c)
 {
     constexpr uintptr_t vmask = 8 * D::bytes - 1;
@@ -167,6 +245,22 @@ static cudaError_t launch_t(const SumArgs& a, const LaunchCfg& c)
         aligned = aligned && ((uintptr_t)a.in[r] & vmask) == 0;
     const int threads = 256;
     void* args[] = {const_cast<SumArgs*>(&a)};
+    const int rmax = a.R <= 2 ? 2 : a.R <= 4 ? 4 : a.R <= 8 ? 8 : 16;
+    if (!aligned && D::bytes == 2) {
+        // elements before the output's first 16-byte boundary, then whole vectors
+        const uint64_t h = ((16u - ((uintptr_t)a.out & 15u)) & 15u) / 2u;
+        const uint64_t nv = a.n > h ? (a.n - h) / 8 : 0;
+        if (nv >= 3) {
+            const void* fn = shift_fn<D>(rmax);
+            uint64_t blocks = (nv - 2 + threads - 1) / threads;
+            const uint64_t cap = (uint64_t)c.sms * 8;
+            if (blocks > cap)
+                blocks = cap;
+            uint64_t hh = h, nvv = nv;
+            void* sargs[] = {const_cast<SumArgs*>(&a), &hh, &nvv};
+            return cudaLaunchKernel(fn, dim3((unsigned)blocks), dim3(threads), sargs, 0, c.stream);
+        }
+    }
     if (!aligned) {
         uint64_t blocks = (a.n + threads - 1) / threads;
         const uint64_t cap = (uint64_t)c.sms * 8;
@@ -177,7 +271,6 @@ static cudaError_t launch_t(const SumArgs& a, const LaunchCfg& c)
         return cudaLaunchKernel((const void*)vector_sum_scalar_kernel<D>, dim3((unsigned)blocks),
                                 dim3(threads), args, 0, c.stream);
     }
-    const int rmax = a.R <= 2 ? 2 : a.R <= 4 ? 4 : a.R <= 8 ? 8 : 16;
     const void* fn = sum_fn<D>(rmax);
     // blocks per SM, per type and RMAX (atomic: calls may come from several
     // host threads; every writer stores the same value)

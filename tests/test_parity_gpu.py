@@ -587,6 +587,30 @@ def test_vector_sum_ranks_types_and_misaligned(R, N, dtype, offset):
     assert bool((out_full[offset + N:] == 0).all())
 
 
+@pytest.mark.parametrize("R,N,dtype,acc", [(8, 1_000_003, "fp16", 0), (3, 4099, "bf16", 0),
+                                            (16, 77777, "fp16", 1), (5, 12345, "bf16", 1),
+                                            (2, 40, "fp16", 0), (1, 33, "bf16", 0),
+                                            (8, 25, "fp16", 0)])
+def test_vector_sum_realigned_inputs(R, N, dtype, acc):
+    """Every rank and the output at its own element offset (0..7): the inputs
+    are read as aligned 16-byte blocks and realigned in registers; results
+    bit-exact, nothing outside the output written."""
+    rng = np.random.default_rng(R * 1000 + N)
+    offs = rng.integers(0, 8, size=R)
+    oo = int(rng.integers(0, 8))
+    x = W.make_sum_inputs(W.SumWorkload("s", R=R, N=N + 8, dtype=dtype))
+    views = np.stack([W.bits(x[r, offs[r]:offs[r] + N]) for r in range(R)])
+    exp = oracle.vector_sum(PY.ODT[dtype], views, acc=acc)
+    xd = x.cuda()
+    out_full = torch.full((N + 16,), 7.0, dtype=xd.dtype, device="cuda")
+    out = out_full[oo:oo + N]
+    B.ar_fusion_sum_ex([xd[r, int(offs[r]):int(offs[r]) + N] for r in range(R)], out,
+                       accumulate=B.AR_ACC_ELEMENT if acc else B.AR_ACC_FP32)
+    torch.cuda.synchronize()
+    assert np.array_equal(W.bits(out.cpu()), exp), np.count_nonzero(W.bits(out.cpu()) != exp)
+    assert bool((out_full[:oo] == 7.0).all()) and bool((out_full[oo + N:] == 7.0).all())
+
+
 # ------------------------------------------- NVFP4 scales in the tile layout
 
 def _run_nvfp4_swizzled(w, variant, inp=None, gs=None):
