@@ -331,6 +331,28 @@ class GraphTimer:
     def cold(self, body):
         return self.warm(lambda: (self.flush(), body())) - self.warm(self.flush)
 
+    def cold_call(self, body, reps=20):
+        """The call alone on evicted inputs: flush, event, call, event, queued
+        back to back (the flush keeps the queue ahead of the GPU, so the
+        events bracket the call); median over `reps`.  Unlike cold(), the
+        write-back of the call's outputs still dirty in L2 when it ends is
+        not charged to it."""
+        torch = self.torch
+        cur = torch.cuda.current_stream(self.dev)
+        for _ in range(3):
+            self.flush()
+            body()
+        torch.cuda.synchronize(self.dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)]
+        for a, b in ev:
+            self.flush()
+            a.record(cur)
+            body()
+            b.record(cur)
+        torch.cuda.synchronize(self.dev)
+        return _median([a.elapsed_time(b) * 1e3 for a, b in ev])
+
 
 def run_sweep(args):
     """Per-workload device time of one call (CUDA graphs of repeated calls,
@@ -446,12 +468,16 @@ def run_sweep(args):
             parts = [P[r] for r in range(w.R)]
             us = cold_us(lambda: B.ar_fusion_run(ws, parts, X, G, w.eps, pat, out["res"],
                                                  out["norm"], q, sf, sc))
+            cc = timer.cold_call(lambda: B.ar_fusion_run(
+                ws, parts, X, G, w.eps, pat, out["res"], out["norm"], q, sf, sc)) if us > 20 else None
             rc, _ = B.ar_fusion_workspace_status(ws)
             byts = fused_bytes(w, pat)
             print(json.dumps({"sweep": w.name, "dtype": w.dtype, "mode": "caller partials",
                               "us": us, "tokens_per_s": w.T / (us * 1e-6), "bytes": byts,
                               "gbs": byts / (us * 1e-6) / 1e9,
                               "frac_of_copy_peak": byts / (us * 1e-6) / 1e9 / peak,
+                              "call_us": cc,
+                              "call_frac": cc and byts / (cc * 1e-6) / 1e9 / peak,
                               "l2": f"cold: {3 * l2_bytes / 1e6:.0f} MB read between calls",
                               "status": rc}), flush=True)
         B.ar_fusion_workspace_destroy(ws)
@@ -623,7 +649,15 @@ def run_configs(timer, peak, dev, B, W, clocks=None):
             e["cold"] = {"us": uc, "tokens_per_s": w.T / (uc * 1e-6),
                          "gbs": byts / (uc * 1e-6) / 1e9, "frac": byts / (uc * 1e-6) / 1e9 / peak,
                          "l2": f"caller partials, {3 * timer.l2_bytes / 1e6:.0f} MB read "
-                               "before every call"}
+                               "before every call; includes the write-back of outputs still "
+                               "dirty in L2 when the call ends"}
+            if us > 20.0:
+                # long enough for the few microseconds of an event pair not to matter
+                cc = timer.cold_call(lambda: B.ar_fusion_run(ws, parts, X, G, w.eps, pat, res,
+                                                             nrm, q, None, sc))
+                e["cold"].update({"call_us": cc, "call_frac": byts / (cc * 1e-6) / 1e9 / peak,
+                                  "call_l2": "the call alone between CUDA events after the "
+                                             "same read"})
         if clocks is not None:
             ck = clocks.summary(t0, time.time())
             e["clocks"] = {"sm_mhz": ck.get("sm_mhz"), "samples": ck.get("samples"),
