@@ -381,6 +381,50 @@ def test_bulk_pipe_with_a_1ns_wait_bound_is_correct_or_reports_a_timeout():
     B.ar_fusion_workspace_destroy(ws)
 
 
+def test_lamport_wait_times_out_in_the_pipelined_row_and_reset_recovers():
+    """At most 4 ranks, one vector per thread: the row's rank vectors are
+    loaded ahead and polled in place.  A rank that never arrives makes that
+    poll give up (AR_ERR_TIMEOUT naming the row and the rank); after a reset
+    the workspace computes the oracle's outputs."""
+    w = W.FusedWorkload("lam_pipe_timeout", R=4, T=64, H=4096, pattern=W.RES_NORM_FP8)
+    inp = W.make_fused_inputs(w)
+    ws = make_ws(w)
+    B.ar_fusion_workspace_set_variant(ws, B.AR_VARIANT_CTA_ROW)
+    B.ar_fusion_workspace_set_timeout_ns(ws, 20_000_000)    # 20 ms bound per wait
+    P = inp.partials.cuda()
+    X, G = inp.residual.cuda(), inp.gamma.cuda()
+    res, nrm = torch.empty_like(X), torch.empty_like(X)
+    q = torch.empty(w.T, w.H, dtype=torch.uint8, device="cuda")
+    sc = torch.ones(1, device="cuda")
+    for r in range(w.R - 1):                # rank 3 never arrives
+        B.ar_fusion_workspace_stage(ws, r, P[r])
+    B.ar_fusion_run(ws, None, X, G, w.eps, B.PATTERNS[w.pattern], residual_out=res, norm_out=nrm,
+                    quant_out=q, scale_factor=sc)
+    rc, detail = B.ar_fusion_workspace_status(ws)
+    assert rc == B.AR_ERR_TIMEOUT
+    assert detail % 32 == w.R - 1 and 0 <= detail // 32 < w.T
+    assert B.ar_fusion_workspace_info(ws)["last_variant"] == B.AR_VARIANT_CTA_ROW
+    B.ar_fusion_workspace_reset(ws)
+    B.ar_fusion_workspace_set_timeout_ns(ws, 2_000_000_000)
+    exp = PY.oracle_expected(w, inp, lamport_flip=True)
+    got = PY.run_gpu(ws, w, inp, scale=exp["scale"], staged=True)
+    PY.check_all(w, got, exp)
+    assert B.ar_fusion_workspace_status(ws)[0] == 0
+    B.ar_fusion_workspace_destroy(ws)
+
+
+@pytest.mark.parametrize("R,T,H,dtype", [(4, 400, 4096, "bf16"), (2, 700, 8192, "fp16"),
+                                         (3, 333, 2064, "bf16")])
+def test_forced_lamport_with_several_rows_per_block(R, T, H, dtype):
+    """Lamport mode forced beyond the one-shot token count: every block runs
+    several rows, so the look-ahead loads of the next row are polling loads
+    of the current slot."""
+    w = W.FusedWorkload(f"lam_rows_{R}_{T}_{H}", R=R, T=T, H=H, dtype=dtype,
+                        pattern=W.RES_NORM_NVFP4, seed=R + T)
+    stats, _, _ = run_and_check(w, B.AR_VARIANT_CTA_ROW, staged=True, mode=B.AR_MODE_LAMPORT)
+    assert stats["residual_mismatch"] == 0, stats
+
+
 # --------------------------------------------------------------- ABI errors
 
 def test_abi_errors_launch_nothing():
