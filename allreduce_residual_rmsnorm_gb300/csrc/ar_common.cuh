@@ -496,6 +496,20 @@ __host__ __device__ __forceinline__ void two_sum(float a, float b, float& s, flo
     err = rn_add(rn_add(a, -rn_add(s, -bb)), rn_add(b, -bb));
 }
 
+// a += t for a non-negative running sum and term (sums of squares): ordering
+// the two by max / min makes Dekker's fast two-sum exact (three additions
+// instead of TwoSum's six); the new high part is hi + t itself, so a NaN term
+// propagates.
+__host__ __device__ __forceinline__ void df_add_nonneg(DF& a, float t)
+{
+    const float s = rn_add(a.hi, t);
+    const float big = fmaxf(a.hi, t);
+    const float small = fminf(a.hi, t);
+    const float err = rn_add(rn_add(big, -s), small);
+    a.hi = s;
+    a.lo = rn_add(a.lo, err);
+}
+
 // Pair addition: the high parts are added exactly (TwoSum) and every rounding
 // error lands in lo; lo is not renormalised into hi between steps (its own
 // rounding errors are ~2^-24 of an already tiny value), which keeps the

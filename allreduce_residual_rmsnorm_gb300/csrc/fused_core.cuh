@@ -26,19 +26,20 @@ __device__ __forceinline__ typename D::Vec residual_vec(const float (&s)[8],
         unpack8<D>(pack8<D>(s), a);
         add8<D>(a, x);
         const typename D::Vec y = pack8<D>(a);
+        // one scalar lane (the other stays zero) by the fast two-sum of
+        // non-negative terms: packed pairs measured slower here (fp32, R = 4,
+        // T = 8192, H = 4096: 161.2 vs 132.7 us), and a second lane or TwoSum's
+        // extra additions cost 2-4% in the wide fp32 bulk-copy pipe
+        DF acc = {ss.hi.x, ss.lo.x};
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            // scalar lanes: packed pairs measured slower here (fp32, R = 4,
-            // T = 8192, H = 4096: 161.2 vs 132.7 us)
-            float& hi = (i & 1) ? ss.hi.y : ss.hi.x;
-            float& lo = (i & 1) ? ss.lo.y : ss.lo.x;
             const float p = __fmul_rn(a[i], a[i]);
             const float e = __fmaf_rn(a[i], a[i], -p);
-            float sum, err;
-            two_sum(hi, p, sum, err);
-            hi = sum;
-            lo = __fadd_rn(__fadd_rn(lo, err), e);
+            df_add_nonneg(acc, p);
+            acc.lo = __fadd_rn(acc.lo, e);
         }
+        ss.hi.x = acc.hi;
+        ss.lo.x = acc.lo;
         return y;
     } else {
         // a = rnd(s); y = rnd(f(a) + f(x)) by packed 16-bit adds
@@ -126,6 +127,25 @@ __device__ __forceinline__ size_t sf_offset(int layout, int m, int k, int kblock
     return tile * 512 + (size_t)(m & 31) * 16 + (size_t)((m >> 5) & 3) * 4 + (size_t)(k & 3);
 }
 
+// t = x * k per element (rounded to fp32), in packed pairs for 16-bit elements
+template <class D>
+__device__ __forceinline__ void scale8(const float (&x)[8], float k, float (&t)[8])
+{
+    if constexpr (D::bytes == 2) {
+        const F2 k2 = {k, k};
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+            const F2 v = f2_mul(F2{x[i], x[i + 1]}, k2);
+            t[i] = v.x;
+            t[i + 1] = v.y;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            t[i] = __fmul_rn(x[i], k);
+    }
+}
+
 // n = rnd((f(y) * rstd) * gamma); stores norm_out and the quantised outputs
 // of vector v of `row`.  Every lane of the warp must call this (the NVFP4
 // block maximum is exchanged with the xor-1 neighbour); `ok` masks the stores
@@ -139,12 +159,20 @@ __device__ __forceinline__ void normalize_vec(const FusedArgs& a, int pat, int r
     const int H = a.H;
     float yf[8], nf[8];
     unpack8<D>(y, yf);
-    const F2 r2 = {rstd, rstd};
+    if constexpr (D::bytes == 2) {
+        // packed pairs (fp32 elements keep scalar products: the packed form
+        // measured 3-4% slower in the wide fp32 bulk-copy pipe)
+        const F2 r2 = {rstd, rstd};
 #pragma unroll
-    for (int i = 0; i < 8; i += 2) {
-        const F2 n = f2_mul(f2_mul(F2{yf[i], yf[i + 1]}, r2), F2{g[i], g[i + 1]});
-        nf[i] = n.x;
-        nf[i + 1] = n.y;
+        for (int i = 0; i < 8; i += 2) {
+            const F2 n = f2_mul(f2_mul(F2{yf[i], yf[i + 1]}, r2), F2{g[i], g[i + 1]});
+            nf[i] = n.x;
+            nf[i + 1] = n.y;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            nf[i] = __fmul_rn(__fmul_rn(yf[i], rstd), g[i]);
     }
     const typename D::Vec nv = pack8<D>(nf);
     if (ok && (pat & AR_NORM_OUT))
@@ -160,13 +188,7 @@ __device__ __forceinline__ void normalize_vec(const FusedArgs& a, int pat, int r
     }
     if (pat & AR_QUANT_FP8) {
         float t[8];
-        const F2 q2 = {qscale, qscale};
-#pragma unroll
-        for (int i = 0; i < 8; i += 2) {
-            const F2 v = f2_mul(F2{nq[i], nq[i + 1]}, q2);
-            t[i] = v.x;
-            t[i + 1] = v.y;
-        }
+        scale8<D>(nq, qscale, t);
         const uint2 c = e4m3x8(t);
         if (ok)
             st_u2(a.quant_out + (size_t)row * H + (size_t)v * 8, c.x, c.y);
@@ -180,13 +202,7 @@ __device__ __forceinline__ void normalize_vec(const FusedArgs& a, int pat, int r
         const float dec = e4m3_to_f32(sf);
         const float enc = dec == 0.0f ? 0.0f : __fdiv_rn(qscale, dec);
         float t[8];
-        const F2 e2 = {enc, enc};
-#pragma unroll
-        for (int i = 0; i < 8; i += 2) {
-            const F2 v = f2_mul(F2{nq[i], nq[i + 1]}, e2);
-            t[i] = v.x;
-            t[i + 1] = v.y;
-        }
+        scale8<D>(nq, enc, t);
         const uint32_t codes = e2m1x8(t);
         if (ok) {
             *reinterpret_cast<uint32_t*>(a.quant_out + (size_t)row * (H / 2) + (size_t)v * 4) = codes;

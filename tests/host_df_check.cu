@@ -5,7 +5,9 @@
 // the merge of the two lanes, then a butterfly of df_add as in a warp
 // reduction must give the exact sum of squares rounded once to fp32, with
 // every lane of the butterfly ending on the same bits.
-// Built with -DAR_DF_CHECK_PLANT=1 the accumulation drops the TwoSum errors
+// The same for one lane accumulated by the fast two-sum of non-negative
+// terms (df_add_nonneg, the fp32-element form).
+// Built with -DAR_DF_CHECK_PLANT=1 the accumulation drops the rounding errors
 // (a plain fp32 sum of the terms): that build must fail the check.
 #include <cstdio>
 #include <cstdlib>
@@ -41,22 +43,29 @@ int main()
         float y = bf16_trunc(ldexpf(1.0f + (mag(rng) + 8.0f) / 16.0f, (int)mag(rng)));
         return sign(rng) ? -y : y;
     };
-    for (int trial = 0; trial < 800; ++trial) {
+    for (int trial = 0; trial < 1600; ++trial) {
+        const bool one_lane = trial >= 800;
         const int lanes = 32, per = 8 * (1 + (trial / 2) % 32);  // up to 8192 terms per row
         DF acc[32];
         long double exact = 0.0L;
         for (int l = 0; l < lanes; ++l) {
             DF2 a2 = {};
+            DF a1 = {0.0f, 0.0f};
             for (int i = 0; i < per; i += 2) {
                 const float y0 = draw(), y1 = draw();
                 const F2 t = {y0 * y0, y1 * y1};             // exact: 8-bit significands
                 exact += (long double)t.x + (long double)t.y;
-                if (AR_DF_CHECK_PLANT)
+                if (AR_DF_CHECK_PLANT) {
                     a2.hi = arf::f2_add(a2.hi, t);
-                else
+                    a1.hi = a1.hi + t.x + t.y;
+                } else if (one_lane) {
+                    arf::df_add_nonneg(a1, t.x);
+                    arf::df_add_nonneg(a1, t.y);
+                } else {
                     arf::df2_add_terms(a2, t);
+                }
             }
-            acc[l] = arf::df2_merge(a2);
+            acc[l] = one_lane ? a1 : arf::df2_merge(a2);
         }
         for (int m = 16; m >= 1; m >>= 1) {                  // xor butterfly
             DF nxt[32];

@@ -25,7 +25,7 @@ def test_double_float_check_rejects_a_plain_fp32_sum(tmp_path):
     r = _df_check(tmp_path, 1)
     assert r.returncode != 0
     bad = int(r.stdout.strip().split()[0].split("/")[0])
-    assert bad > 400, r.stdout
+    assert bad > 800, r.stdout
 
 
 # ---- the packed 16-bit residual add: rnd16(fp32(a + b)) == rnd16(a + b)
