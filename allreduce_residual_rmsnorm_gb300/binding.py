@@ -341,6 +341,33 @@ def ar_fusion_run(ws: Workspace, partials, residual_in: torch.Tensor, gamma: tor
                                _ptr(scale_out), _ptr(scale_factor), _stream(stream)))
 
 
+def bound_run(ws: Workspace, partials, residual_in: torch.Tensor, gamma: torch.Tensor,
+              eps: float, pattern: int, residual_out=None, norm_out=None, quant_out=None,
+              scale_out=None, scale_factor=None, stream=None, nranks: int | None = None):
+    """ar_fusion_run with every argument marshalled once: returns a callable
+    that launches the call (same tensors, same stream) with no per-call
+    Python work beyond the C call itself, for loops that repeat one call.
+    The tensors must stay alive while the callable is used."""
+    tokens, hidden = residual_in.shape[0], residual_in.shape[-1]
+    if partials is None:
+        parr = None
+        R = ws.tp_size if nranks is None else nranks
+    else:
+        parr = _ptr_array(partials)
+        R = len(partials) if nranks is None else nranks
+    fn = lib().ar_fusion_run
+    args = (ws.handle, parr, R, tokens, hidden, _dtype_id(residual_in), _ptr(residual_in),
+            _ptr(gamma), ctypes.c_float(eps), pattern, _ptr(residual_out), _ptr(norm_out),
+            _ptr(quant_out), _ptr(scale_out), _ptr(scale_factor), _stream(stream))
+
+    def call():
+        rc = fn(*args)
+        if rc != AR_OK:
+            _check(rc)
+
+    return call
+
+
 def ar_fusion_norm_amax(ws: Workspace, partials, residual_in: torch.Tensor, gamma: torch.Tensor,
                         eps: float, amax_out: torch.Tensor, stream=None,
                         nranks: int | None = None) -> None:

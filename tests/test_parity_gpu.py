@@ -425,6 +425,37 @@ def test_forced_lamport_with_several_rows_per_block(R, T, H, dtype):
     assert stats["residual_mismatch"] == 0, stats
 
 
+def test_bound_run_repeats_the_call_it_was_made_for():
+    """binding.bound_run marshals the arguments once; calling it launches the
+    same call: the oracle's outputs, three times in a row on staged partials."""
+    w = W.FusedWorkload("bound", R=8, T=300, H=7168, pattern=W.RES_QUANT_NVFP4, heavy_frac=0.01)
+    inp = W.make_fused_inputs(w)
+    exp = PY.oracle_expected(w, inp)
+    ws = make_ws(w)
+    P = inp.partials.cuda()
+    X, G = inp.residual.cuda(), inp.gamma.cuda()
+    for r in range(w.R):
+        B.ar_fusion_workspace_stage(ws, r, P[r], mode=B.AR_MODE_BUFFER)
+    res = torch.empty_like(X)
+    q = torch.empty(w.T, w.H // 2, dtype=torch.uint8, device="cuda")
+    sf = torch.empty(w.T, w.H // 16, dtype=torch.uint8, device="cuda")
+    sc = torch.tensor([float(exp["scale"])], device="cuda")
+    call = B.bound_run(ws, None, X, G, w.eps, B.PATTERNS[w.pattern], residual_out=res,
+                       quant_out=q, scale_out=sf, scale_factor=sc)
+    B.ar_fusion_workspace_set_mode(ws, B.AR_MODE_BUFFER)
+    for _ in range(3):
+        res.fill_(float("nan"))
+        q.fill_(0xAA)
+        sf.fill_(0xAA)
+        call()
+        torch.cuda.synchronize()
+        got = {"residual": W.bits(res.cpu()), "quant": q.cpu().numpy(), "sf": sf.cpu().numpy()}
+        PY.check_all(w, got, exp)
+        assert np.array_equal(got["residual"], exp["residual"])
+    assert B.ar_fusion_workspace_status(ws)[0] == 0
+    B.ar_fusion_workspace_destroy(ws)
+
+
 # --------------------------------------------------------------- ABI errors
 
 def test_abi_errors_launch_nothing():
