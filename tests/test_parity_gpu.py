@@ -686,6 +686,27 @@ def test_vector_sum_realigned_inputs(R, N, dtype, acc):
     assert bool((out_full[:oo] == 7.0).all()) and bool((out_full[oo + N:] == 7.0).all())
 
 
+@pytest.mark.parametrize("R,N,dtype,acc,pad", [(3, (1 << 25) + 13, "bf16", 0, 16),
+                                                (8, (1 << 25) + 13, "fp16", 1, 16),
+                                                (2, (1 << 25) + 5, "fp16", 0, 8)])
+def test_vector_sum_large_sizes_with_32_byte_rows(R, N, dtype, acc, pad):
+    """From 2^25 elements, 16-bit sums over 32-byte aligned buffers read 256
+    bits per load (ragged tail summed element by element); rows aligned to 16
+    bytes only (pad = 8 elements) keep the 128-bit path.  Bit-exact."""
+    stride = (N + pad - 1) // pad * pad
+    x = W.make_sum_inputs(W.SumWorkload("s", R=R, N=stride, dtype=dtype))
+    exp = oracle.vector_sum(PY.ODT[dtype], W.bits(x[:, :N]), acc=acc)
+    xd = x.cuda()
+    out_full = torch.full((stride + 16,), 7.0, dtype=xd.dtype, device="cuda")
+    out = out_full[:N]
+    B.ar_fusion_sum_ex([xd[r, :N] for r in range(R)], out,
+                       accumulate=B.AR_ACC_ELEMENT if acc else B.AR_ACC_FP32)
+    torch.cuda.synchronize()
+    got = W.bits(out.cpu())
+    assert np.array_equal(got, exp), np.count_nonzero(got != exp)
+    assert bool((out_full[N:] == 7.0).all())
+
+
 # ------------------------------------------- NVFP4 scales in the tile layout
 
 def _run_nvfp4_swizzled(w, variant, inp=None, gs=None):
