@@ -37,18 +37,25 @@ __host__ __device__ constexpr int one_vec_threads(int rmax)
 }
 
 // Block size bound: one_vec_threads for one vector per thread; wider rows
-// (several vectors per thread) at most 512; one row per warp: 8 warps.
-template <class D, int RMAX, int VPT, bool WARP_ROW>
+// (several vectors per thread) and the two-rows-per-SM form at most 512; one
+// row per warp: 8 warps.
+template <class D, int RMAX, int VPT, bool WARP_ROW, bool LIGHT = false, bool AHEAD = false>
 constexpr int rows_max_threads()
 {
-    return WARP_ROW ? 256 : (VPT == 1 ? one_vec_threads<D>(RMAX) : 512);
+    return WARP_ROW ? 256 : (LIGHT || AHEAD) ? 512 : (VPT == 1 ? one_vec_threads<D>(RMAX) : 512);
 }
 
-// LIGHT, two rows per SM: 16-bit rows of 513..1024 vectors with at most 4
-// ranks run as blocks of <= 512 threads at two vectors per thread and one
-// vector per load batch, within 64 registers, so that two blocks (two rows)
-// share an SM and one row's reductions overlap the other's loads (the
-// launcher picks this for light rows, see launch_fused_rows_t).
+// LIGHT, two rows per SM: blocks of <= 512 threads within 64 registers, so
+// that two blocks (two rows) share an SM and one row's reductions overlap the
+// other's loads.  Two forms (the launcher picks them, see
+// launch_fused_rows_t): 16-bit rows of 513..1024 vectors with at most 4
+// ranks at two vectors per thread and one vector per load batch, and 16-bit
+// rows of 449..512 vectors with 5 ranks at one vector per thread (whose
+// unbounded build takes more than 64 registers, one block per SM).
+// AHEAD: one vector per thread with 5..8 ranks in blocks of <= 512 threads,
+// whose register budget (up to 128) holds the next row's eight rank vectors
+// and residual vector: the look-ahead below, otherwise taken only with at
+// most 4 ranks.
 template <bool LIGHT>
 __host__ __device__ constexpr int rows_min_blocks()
 {
@@ -88,8 +95,9 @@ __device__ __forceinline__ void fold_ranks(float (&s)[KCH][8],
 // CLUSTER: the kernel is launched with a thread-block cluster and one row
 // spans its CTAs (a separate instantiation, so the common one-CTA-per-row
 // kernel carries none of the cluster code).
-template <class D, int RMAX, int VPT, bool WARP_ROW, bool CLUSTER = false, bool LIGHT = false>
-__global__ void __launch_bounds__(rows_max_threads<D, RMAX, VPT, WARP_ROW>(),
+template <class D, int RMAX, int VPT, bool WARP_ROW, bool CLUSTER = false, bool LIGHT = false,
+          bool AHEAD = false>
+__global__ void __launch_bounds__(rows_max_threads<D, RMAX, VPT, WARP_ROW, LIGHT, AHEAD>(),
                                   rows_min_blocks<LIGHT>())
 fused_rows_kernel(const FusedArgs a)
 {
@@ -107,8 +115,13 @@ fused_rows_kernel(const FusedArgs a)
     constexpr int RB = RMAX < RBMAX ? RMAX : RBMAX;
     // vectors per batch (one in the two-rows-per-SM form)
     constexpr int KCH = LIGHT ? 1 : ((LOADS / RB) > VPT ? VPT : (LOADS / RB));
-    static_assert(!LIGHT || (D::bytes == 2 && VPT == 2 && RMAX <= 4 && !WARP_ROW && !CLUSTER),
-                  "two rows per SM: 16-bit, two vectors per thread, at most 4 ranks");
+    static_assert(!LIGHT || (D::bytes == 2 && !WARP_ROW && !CLUSTER &&
+                             ((VPT == 2 && RMAX <= 4) || (VPT == 1 && RMAX == 8))),
+                  "two rows per SM: 16-bit; two vectors per thread with at most 4 ranks, "
+                  "or one vector per thread with 5..8");
+    static_assert(!AHEAD || (D::bytes == 2 && VPT == 1 && RMAX == 8 && !WARP_ROW && !CLUSTER &&
+                             !LIGHT),
+                  "look-ahead of 5..8 ranks: 16-bit, one vector per thread, <= 512 threads");
     static_assert(VPT % KCH == 0, "batch must divide VPT");
     static_assert(RMAX % RB == 0, "rank batch must divide RMAX");
 
@@ -186,9 +199,11 @@ fused_rows_kernel(const FusedArgs a)
     // 120.3 / 131.2.  With 8 or 16 ranks the 896-thread blocks have registers
     // for two ranks ahead only, which measured slower (R=8, H=7168: 180 ->
     // 221 us), so those rows load as before; so did two vectors per thread
-    // at 512 threads with the same look-ahead (R=4, H=8192: 65.9 us).  The
-    // row then works on `pre` / `pre_x` in place (no register copies).
-    constexpr bool PIPE = !WARP_ROW && !CLUSTER && VPT == 1 && RMAX <= 4;
+    // at 512 threads with the same look-ahead (R=4, H=8192: 65.9 us).  Rows
+    // of <= 512 vectors with 6..8 ranks take it in the AHEAD instantiation
+    // (R=8, T=8192, H=4096: 116.9 -> 109.4 us).  The row then works on
+    // `pre` / `pre_x` in place (no register copies).
+    constexpr bool PIPE = !WARP_ROW && !CLUSTER && VPT == 1 && (RMAX <= 4 || AHEAD);
     V pre[KCH][RB];
     V pre_x[KCH];
     const auto load_first = [&](int r_) {

@@ -32,7 +32,8 @@ static const void* rows_fn_vpt(int vpt)
     }
 }
 
-// two rows per SM (16-bit, at most 4 ranks, two vectors per thread)
+// two rows per SM (16-bit): two vectors per thread with at most 4 ranks, one
+// vector per thread with 5..8
 template <class D>
 static const void* rows_light_fn(int rmax)
 {
@@ -40,9 +41,18 @@ static const void* rows_light_fn(int rmax)
         switch (rmax) {
         case 2: return (const void*)fused_rows_kernel<D, 2, 2, false, false, true>;
         case 4: return (const void*)fused_rows_kernel<D, 4, 2, false, false, true>;
+        case 8: return (const void*)fused_rows_kernel<D, 8, 1, false, false, true>;
         default: return nullptr;
         }
     }
+    return nullptr;
+}
+
+template <class D>
+static const void* rows_ahead_fn()
+{
+    if constexpr (D::bytes == 2)
+        return (const void*)fused_rows_kernel<D, 8, 1, false, false, false, true>;
     return nullptr;
 }
 
@@ -176,6 +186,32 @@ cudaError_t launch_fused_rows_t(int variant, const FusedArgs& a, const LaunchCfg
             vpt = 2;
             light = true;
         }
+        // 16-bit rows of 449..512 vectors with 5..8 ranks: the one-vector
+        // kernel takes 68 registers there, one block of 480..512 threads per
+        // SM, and with 8 ranks it has no registers for the next row's
+        // loads.  At most 512 threads leave up to 128 registers: with 6..8
+        // ranks the next row's rank and residual vectors are loaded ahead as
+        // for <= 4 ranks (114 registers); with 5 ranks two blocks of <= 64
+        // registers share the SM instead.  Measured (us, back-to-back /
+        // inputs evicted; before -> 64 registers -> look-ahead), T=8192,
+        // H=4096, residual + norm: R=8 116.9 / 129.1 -> 118.1 / 125.4 ->
+        // 109.4 / 116.6 (0.99 of the copy bandwidth); R=7 109.9 / 121.4 ->
+        // 107.8 / 115.8 -> 102.2 / 109.1; R=6 106.9 / 119.2 -> 96.0 / 106.3
+        // -> 95.7 / 104.4; R=5 103.3 / 115.6 -> 86.5 / 96.8 -> 90.7 / 100.7.
+        // R=8 with NVFP4 output 133.3 -> 120.5 -> 114.5, with FP8 output
+        // 122.8 -> 124.4 -> 115.4; R=8, T=512 9.3 / 15.4 -> 8.3 / 15.3 ->
+        // 8.8 / 13.0.  Narrower rows already hold two or more 68-register
+        // blocks per SM, and neither form wins there (look-ahead, R=8:
+        // H=1024 114.2 -> 108.4, H=2048 112.2 -> 108.6, but with NVFP4
+        // output 107.8 -> 114.4, H=1536 86.5 -> 92.8, H=2560 136.3 -> 180.5;
+        // 64 registers: H=3072 86.3 -> 96.0), so they keep the plain kernel.
+        bool ahead = false;
+        if (D::bytes == 2 && C == 1 && rmax == 8 && Hv > 448 && Hv <= 512) {
+            if (a.R >= 6 && a.T > c.sms)
+                ahead = true;
+            else if (a.T >= 2 * c.sms)
+                light = true;
+        }
         // 1025..1536 vectors of a 16-bit row with at most 4 ranks: three
         // vectors per thread (up to 512 threads) instead of four (up to 384);
         // measured R=2, H=10240, T=16384: 256.4 vs 312.3 us; R=4, H=10240,
@@ -185,7 +221,8 @@ cudaError_t launch_fused_rows_t(int variant, const FusedArgs& a, const LaunchCfg
         if (vpt > 8)
             return cudaErrorInvalidValue;
         fn = light ? rows_light_fn<D>(rmax)
-                   : (C > 1 && vpt == 1) ? rows_cluster_fn<D>(rmax) : rows_fn<D, false>(rmax, vpt);
+             : ahead ? rows_ahead_fn<D>()
+             : (C > 1 && vpt == 1) ? rows_cluster_fn<D>(rmax) : rows_fn<D, false>(rmax, vpt);
         if (vpt != 1)
             C = 1;
         threads = ((Hv + C * vpt - 1) / (C * vpt) + 31) / 32 * 32;

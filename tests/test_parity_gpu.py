@@ -99,6 +99,13 @@ EDGE = [
     # at least 2 rows per SM); the last one stays one row per SM
     (3, 320, 6160, "bf16", W.RES_NORM_NVFP4), (4, 350, 4104, "fp16", W.RES_NORM_FP8),
     (2, 400, 8192, "bf16", W.RES_QUANT_FP8), (4, 333, 8192, "bf16", W.RES_NORM),
+    # 449..512 vectors, one vector per thread: 6..8 ranks load the next row
+    # ahead (more rows than SMs), 5 ranks run two rows per SM (at least 2
+    # rows per SM); the last one has one row per block
+    (8, 320, 4096, "bf16", W.RES_NORM_NVFP4), (6, 400, 3600, "fp16", W.RES_NORM_FP8),
+    (7, 153, 4096, "bf16", W.RES_QUANT_NVFP4), (8, 303, 4096, "fp16", W.RES_NORM),
+    (5, 310, 4000, "bf16", W.RES_NORM), (5, 200, 4096, "fp16", W.RES_NORM),
+    (8, 152, 4096, "bf16", W.RES_NORM),
 ]
 
 
@@ -414,7 +421,8 @@ def test_lamport_wait_times_out_in_the_pipelined_row_and_reset_recovers():
 
 
 @pytest.mark.parametrize("R,T,H,dtype", [(4, 400, 4096, "bf16"), (2, 700, 8192, "fp16"),
-                                         (3, 333, 2064, "bf16")])
+                                         (3, 333, 2064, "bf16"), (8, 350, 4096, "bf16"),
+                                         (6, 200, 3728, "fp16")])
 def test_forced_lamport_with_several_rows_per_block(R, T, H, dtype):
     """Lamport mode forced beyond the one-shot token count: every block runs
     several rows, so the look-ahead loads of the next row are polling loads
