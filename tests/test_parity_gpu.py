@@ -177,6 +177,11 @@ ACC_CASES = [
     (W.FusedWorkload("acc_pipe", R=8, T=400, H=7168, pattern=W.RES_QUANT_NVFP4, heavy_frac=0.01),
      B.AR_VARIANT_BULK_PIPE, False),
     (W.FusedWorkload("acc_r16", R=16, T=33, H=1024, pattern=W.RES_NORM), B.AR_VARIANT_WARP_ROW, False),
+    # 449..512 vectors: 8 ranks load the next row ahead, 5 ranks two rows per SM
+    (W.FusedWorkload("acc_ahead", R=8, T=400, H=4096, pattern=W.RES_NORM_NVFP4),
+     B.AR_VARIANT_AUTO, True),
+    (W.FusedWorkload("acc_two_rows", R=5, T=320, H=3840, dtype="fp16", pattern=W.RES_QUANT_FP8),
+     B.AR_VARIANT_AUTO, False),
 ]
 
 
@@ -739,9 +744,9 @@ def _run_nvfp4_swizzled(w, variant, inp=None, gs=None):
 
 
 @pytest.mark.parametrize("variant", [B.AR_VARIANT_WARP_ROW, B.AR_VARIANT_CTA_ROW, B.AR_VARIANT_BULK_PIPE])
-@pytest.mark.parametrize("T,H", [(200, 512), (300, 7168), (128, 1040)])
-def test_nvfp4_swizzled_scale_layout_matches_oracle(variant, T, H):
-    w = W.FusedWorkload("swz", R=4, T=T, H=H, pattern=W.RES_NORM_NVFP4, heavy_frac=0.01, seed=T + H)
+@pytest.mark.parametrize("R,T,H", [(4, 200, 512), (4, 300, 7168), (4, 128, 1040), (8, 320, 4096)])
+def test_nvfp4_swizzled_scale_layout_matches_oracle(variant, R, T, H):
+    w = W.FusedWorkload("swz", R=R, T=T, H=H, pattern=W.RES_NORM_NVFP4, heavy_frac=0.01, seed=T + H)
     exp, q, sf = _run_nvfp4_swizzled(w, variant)
     assert np.array_equal(q.cpu().numpy(), exp["quant"])
     assert np.array_equal(sf.cpu().numpy(), oracle.swizzle_scales(exp["sf"]))
