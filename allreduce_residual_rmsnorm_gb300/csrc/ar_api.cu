@@ -146,8 +146,13 @@ __global__ void stage_kernel(const uint4* src, uint8_t* region, uint64_t slot_by
     pdl_trigger();
     uint8_t* dst = region + rank_off_bytes;
     if (lamport) {
-        const uint32_t flag = *reinterpret_cast<const volatile uint32_t*>(&st->lamport_flag);
-        dst += (uint64_t)(flag % 3u) * slot_bytes;
+        // one polling load per block (polling loads bypass L1: one per
+        // thread would queue thousands of requests on one L2 line)
+        __shared__ uint32_t flag_sh;
+        if (threadIdx.x == 0)
+            flag_sh = *reinterpret_cast<const volatile uint32_t*>(&st->lamport_flag);
+        __syncthreads();
+        dst += (uint64_t)(flag_sh % 3u) * slot_bytes;
     }
     uint4* d = reinterpret_cast<uint4*>(dst);
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;

@@ -74,7 +74,13 @@ __global__ void noalloc_init_kernel(uint8_t* scratch)
 __global__ void noalloc_stage_kernel(arf::FusedArgs a, uint8_t* scratch, uint64_t plane_vecs)
 {
     ar_fusion_state* st = reinterpret_cast<ar_fusion_state*>(scratch + kStateOff);
-    const uint32_t flag = *reinterpret_cast<volatile uint32_t*>(&st->lamport_flag);
+    // one polling load per block (they bypass L1; one per thread would queue
+    // thousands of requests on one L2 line)
+    __shared__ uint32_t flag_sh;
+    if (threadIdx.x == 0)
+        flag_sh = *reinterpret_cast<volatile uint32_t*>(&st->lamport_flag);
+    __syncthreads();
+    const uint32_t flag = flag_sh;
     uint4* slot = reinterpret_cast<uint4*>(scratch + (uint64_t)(flag % 3u) * kSlotBytes);
     const uint64_t total = plane_vecs * (uint64_t)a.R;
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
