@@ -171,18 +171,23 @@ cudaError_t launch_fused_rows_t(int variant, const FusedArgs& a, const LaunchCfg
         if (C > 1 && (Hv + C - 1) / C > one_vec_max)
             C = 1;
         int vpt = (Hv + C - 1) / C <= one_vec_max ? 1 : pow2_at_least((Hv + 511) / 512);
-        // Light 16-bit rows (513..1024 vectors, at most 4 ranks, at most 3072
-        // rank-vectors = 48 KB of partials per row), with at least two rows
+        // Light 16-bit rows (513..1023 vectors, at most 4 ranks, at most 2304
+        // rank-vectors = 36 KB of partials per row), with at least two rows
         // per SM: two rows per SM at two vectors per thread instead of one
-        // 1024-thread row (decode sizes keep one vector per thread).
-        // Measured (us, back-to-back / inputs evicted): R=3, H=4104, T=8192:
-        // 73.6 / 81.0 vs 100.3 / 111.5; R=2, H=6144: 86.4 / 90.2 vs
-        // 95.1 / 108.2; R=4, H=6144: 111.2 / 116.8 vs 118.8 / 131.5.  Heavier
-        // rows lose (R=4, H=8192, T=8192: 157.5 / 152.5 vs 143.2 / 154.4; at
-        // T=2048 with FP8 output: 46.6 / 52.4 vs 45.3 / 54.5).
+        // row per SM at one vector per thread with the next row loaded ahead.
+        // Measured (us, back-to-back / inputs evicted, T=8192, two rows per
+        // SM vs one): R=3, H=4104 73.6 / 81.0 vs 87.6 / 99.1; R=2, H=6144
+        // 83.7 / 89.1 vs 86.0 / 98.5; R=3, H=6144 95.9 / 104.7 vs 98.2 /
+        // 110.6; R=4, H=4608 88.3 / 89.9 vs 88.2 / 90.0.  Heavier rows do
+        // better with the look-ahead: R=4, H=6144 110.8 / 116.4 vs 105.8 /
+        // 116.1; R=3, H=7168 116.4 / 119.0 vs 107.7 / 119.5; R=3, H=8192
+        // 133.8 / 132.3 vs 118.9 / 129.5; R=2, H=8192 106.9 / 115.5 vs
+        // 103.0 / 114.9.  Between them R=4, H=5120 (100.1 / 98.9 vs 95.0 /
+        // 105.8) and H=5632 (102.3 / 108.8 vs 101.6 / 112.7) split the two
+        // timings and take the look-ahead.
         bool light = false;
-        if (D::bytes == 2 && C == 1 && rmax <= 4 && Hv > 512 && Hv <= 1024 &&
-            a.R * Hv <= 3072 && a.T >= 2 * c.sms) {
+        if (D::bytes == 2 && C == 1 && rmax <= 4 && Hv > 512 && Hv < 1024 &&
+            a.R * Hv <= 2304 && a.T >= 2 * c.sms) {
             vpt = 2;
             light = true;
         }

@@ -95,10 +95,12 @@ EDGE = [
     (3, 7, 10240, "bf16", W.RES_NORM_NVFP4), (4, 33, 12288, "fp16", W.RES_NORM_FP8),
     (2, 9, 8200, "bf16", W.RES_NORM),
     (8, 200, 4096, "bf16", W.RES_NORM_NVFP4), (1, 500, 7168, "fp16", W.RES_QUANT_FP8),
-    # two rows per SM (<= 4 ranks, 513..1024 vectors, <= 3072 rank-vectors,
-    # at least 2 rows per SM); the last one stays one row per SM
-    (3, 320, 6160, "bf16", W.RES_NORM_NVFP4), (4, 350, 4104, "fp16", W.RES_NORM_FP8),
-    (2, 400, 8192, "bf16", W.RES_QUANT_FP8), (4, 333, 8192, "bf16", W.RES_NORM),
+    # two rows per SM (<= 4 ranks, 513..1023 vectors, <= 2304 rank-vectors,
+    # at least 2 rows per SM); the last three stay one row per SM (next row
+    # loaded ahead)
+    (3, 320, 6128, "bf16", W.RES_NORM_NVFP4), (4, 350, 4104, "fp16", W.RES_NORM_FP8),
+    (2, 400, 8184, "bf16", W.RES_QUANT_FP8), (3, 320, 6160, "bf16", W.RES_NORM_NVFP4),
+    (2, 400, 8192, "fp16", W.RES_QUANT_FP8), (4, 333, 8192, "bf16", W.RES_NORM),
     # 449..512 vectors, one vector per thread: 6..8 ranks load the next row
     # ahead (more rows than SMs), 5 ranks run two rows per SM (at least 2
     # rows per SM); the last one has one row per block
