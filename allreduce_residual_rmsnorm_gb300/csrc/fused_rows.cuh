@@ -19,9 +19,9 @@
 //
 // In Lamport mode the partials come from the current workspace slot and are
 // polled (bounded) until no 32-bit word holds the -0.0f sentinel; the
-// retired slot is refilled with the sentinel in the same launch and the last
-// block to finish advances the slot index (LamportComm::update without a
-// spin: an atomic ticket).
+// retired slot is refilled with the sentinel in the same launch and the block
+// that takes the last atomic ticket advances the slot index
+// (LamportComm::update without a spin).
 #pragma once
 
 #include <stddef.h>
@@ -63,6 +63,10 @@ __host__ __device__ constexpr int rows_min_blocks()
 {
     return LIGHT ? 2 : 1;
 }
+
+// Lamport launches of at most this many blocks take their slot ticket right
+// after reading the slot state instead of at the end.
+constexpr unsigned kEarlyTicketBlocks = 64;
 
 // s[kk] (+)= rank batch r0..r0+RB-1 of vector g + (k0 + kk) * G; ELEM rounds
 // every partial sum to the element type.
@@ -162,6 +166,7 @@ fused_rows_kernel(const FusedArgs a)
     // register copy) or, in Lamport mode, slot + r * plane
     uint32_t flag = 0;
     const uint8_t* slot = nullptr;
+    unsigned ticket = 0;
     const size_t plane = (size_t)a.T * H * EB;
     if (a.lamport) {
         // The slot state's first 32 bytes in one load, once per block
@@ -198,6 +203,19 @@ fused_rows_kernel(const FusedArgs a)
             st[1] = st_sh[1];
             st[2] = st_sh[2];
             st_hi = st_sh[3];
+        }
+        // Slot ticket.  The last block to take one advances the state at its
+        // end; a ticket proves only that its block has read the state, so
+        // with few blocks it is taken here and its latency hides behind the
+        // row (Lamport call with PDL, µs: 2 blocks 3.59 -> 3.28, 16 blocks
+        // 5.12 -> 4.72, 64 blocks 5.23 -> 4.94).  With many blocks the
+        // tickets taken at once queue on one word (128 blocks: 6.06 ->
+        // 6.64), so those blocks take theirs at the end.
+        if (gridDim.x <= kEarlyTicketBlocks) {
+            if (WARP_ROW)
+                __syncthreads();   // every warp of the block has read the state
+            if (threadIdx.x == 0)
+                ticket = atomicAdd(&a.state->counter, 1u);
         }
         flag = st[0];
         const uint32_t clear_eb = st[1];
@@ -440,14 +458,16 @@ fused_rows_kernel(const FusedArgs a)
             atomicMax(reinterpret_cast<unsigned int*>(a.amax_out), __float_as_uint(amax_local));
     }
 
-    // Slot state: the last block to finish advances it.  Only the next launch
+    // Slot state: the block holding the last ticket advances it.  Only the next launch
     // reads it, and kernel completion (stream order, or griddepcontrol.wait
     // under programmatic dependent launch) already makes every write of this
     // grid visible there, so no fence is needed (one measured 0.2-0.4 us).
     if (a.lamport) {
-        __syncthreads();
+        const bool early = gridDim.x <= kEarlyTicketBlocks;
+        if (!early)
+            __syncthreads();
         if (threadIdx.x == 0) {
-            const unsigned prev = atomicAdd(&a.state->counter, 1u);
+            const unsigned prev = early ? ticket : atomicAdd(&a.state->counter, 1u);
             if (prev == gridDim.x - 1) {
                 a.state->lamport_flag = (flag + 1u) % 3u;
                 a.state->clear_size = (uint64_t)R * a.T * H;
