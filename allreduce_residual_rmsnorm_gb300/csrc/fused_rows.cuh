@@ -64,9 +64,10 @@ __host__ __device__ constexpr int rows_min_blocks()
     return LIGHT ? 2 : 1;
 }
 
-// Lamport launches of at most this many blocks take their slot ticket right
-// after reading the slot state instead of at the end.
-constexpr unsigned kEarlyTicketBlocks = 64;
+// Lamport launches of at most this many blocks (every launch of the one-shot
+// token range) take their slot ticket right after reading the slot state
+// instead of at the end.
+constexpr unsigned kEarlyTicketBlocks = 128;
 
 // s[kk] (+)= rank batch r0..r0+RB-1 of vector g + (k0 + kk) * G; ELEM rounds
 // every partial sum to the element type.
@@ -205,12 +206,13 @@ fused_rows_kernel(const FusedArgs a)
             st_hi = st_sh[3];
         }
         // Slot ticket.  The last block to take one advances the state at its
-        // end; a ticket proves only that its block has read the state, so
-        // with few blocks it is taken here and its latency hides behind the
-        // row (Lamport call with PDL, µs: 2 blocks 3.59 -> 3.28, 16 blocks
-        // 5.12 -> 4.72, 64 blocks 5.23 -> 4.94).  With many blocks the
-        // tickets taken at once queue on one word (128 blocks: 6.06 ->
-        // 6.64), so those blocks take theirs at the end.
+        // end; a ticket proves only that its block has read the state, so it
+        // is taken here and its latency hides behind the row (Lamport call
+        // with PDL, µs: 2 blocks 3.59 -> 3.28, 16 blocks 5.12 -> 4.72, 64
+        // blocks 5.23 -> 4.94, 128 blocks (R=8, T=128, H=4096) 5.6 -> 5.2-5.3,
+        // R=4 4.55 -> 4.10).  Larger launches (Lamport forced beyond the
+        // one-shot token range) take theirs at the end: tickets taken at
+        // once queue on one word.
         if (gridDim.x <= kEarlyTicketBlocks) {
             if (WARP_ROW)
                 __syncthreads();   // every warp of the block has read the state
