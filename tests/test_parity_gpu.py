@@ -803,11 +803,12 @@ def test_nvfp4_swizzled_output_feeds_a_block_scaled_matmul(T):
 # ------------------------------------------------------------- CUDA graphs
 
 @pytest.mark.parametrize("pdl", [0, 1])
-def test_graph_replay_of_stage_and_run_advances_the_lamport_slots(pdl):
+@pytest.mark.parametrize("w", [W.DECODE.with_(T=64), W.DECODE, W.TINY], ids=["t64", "t128", "tiny"])
+def test_graph_replay_of_stage_and_run_advances_the_lamport_slots(pdl, w):
     # the slot index and clear size live on the device, so a captured
     # stage + run replays correctly: each replay reads the slot its staging
-    # filled and clears the previous one
-    w = W.DECODE.with_(T=64)
+    # filled and clears the previous one (row blocks and one-row-per-warp
+    # blocks; every block takes its slot ticket right after the state read)
     ws = make_ws(w)
     B.ar_fusion_workspace_set_launch(ws, 0, pdl)
     inp0 = W.make_fused_inputs(w)
