@@ -91,6 +91,28 @@ __device__ __forceinline__ typename D::Vec sum_vec(const SumArgs& a,
     return pack8<D>(s);
 }
 
+// One element of the rank-order sum (same adds and roundings as sum_vec);
+// every rank's load is issued before the first add, so the element costs
+// one memory round trip rather than one per rank.
+template <class D, int RMAX>
+__device__ __forceinline__ float sum_elem(const SumArgs& a, uint64_t e)
+{
+    float v[RMAX];
+#pragma unroll
+    for (int r = 0; r < RMAX; ++r)
+        v[r] = r < a.R ? ld_elem<D>(a.in[r], e) : 0.0f;
+    float s = v[0];
+#pragma unroll
+    for (int r = 1; r < RMAX; ++r) {
+        if (r < a.R) {
+            s = __fadd_rn(s, v[r]);
+            if (a.acc)
+                s = round1<D>(s);
+        }
+    }
+    return s;
+}
+
 template <class D, int RMAX>
 __global__ void __launch_bounds__(256) vector_sum_kernel(const SumArgs a)
 {
@@ -123,13 +145,7 @@ __global__ void __launch_bounds__(256) vector_sum_kernel(const SumArgs a)
     const uint64_t tail = a.n - nvec * 8;
     if (tid < tail) {
         const uint64_t e = nvec * 8 + tid;
-        float s = ld_elem<D>(a.in[0], e);
-        for (int r = 1; r < a.R; ++r) {
-            s = __fadd_rn(s, ld_elem<D>(a.in[r], e));
-            if (a.acc)
-                s = round1<D>(s);
-        }
-        st_elem<D>(a.out, e, s);
+        st_elem<D>(a.out, e, sum_elem<D, RMAX>(a, e));
     }
 }
 
@@ -185,13 +201,7 @@ __global__ void __launch_bounds__(256) vector_sum_wide_kernel(const SumArgs a)
     const uint64_t tail = a.n - n16 * 16;
     if (tid < tail) {
         const uint64_t e = n16 * 16 + tid;
-        float s = ld_elem<D>(a.in[0], e);
-        for (int r = 1; r < a.R; ++r) {
-            s = __fadd_rn(s, ld_elem<D>(a.in[r], e));
-            if (a.acc)
-                s = round1<D>(s);
-        }
-        st_elem<D>(a.out, e, s);
+        st_elem<D>(a.out, e, sum_elem<D, RMAX>(a, e));
     }
 }
 
@@ -247,13 +257,7 @@ __global__ void __launch_bounds__(256) vector_sum_shift_kernel(const SumArgs a, 
     const uint64_t n_head = h + 8, tail0 = h + 8 * (nv - 1);
     if (tid < n_head + (a.n - tail0)) {
         const uint64_t e = tid < n_head ? tid : tail0 + (tid - n_head);
-        float s = ld_elem<D>(a.in[0], e);
-        for (int r = 1; r < a.R; ++r) {
-            s = __fadd_rn(s, ld_elem<D>(a.in[r], e));
-            if (a.acc)
-                s = round1<D>(s);
-        }
-        st_elem<D>(a.out, e, s);
+        st_elem<D>(a.out, e, sum_elem<D, RMAX>(a, e));
     }
 }
 
