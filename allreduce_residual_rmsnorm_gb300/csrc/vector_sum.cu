@@ -91,16 +91,22 @@ __device__ __forceinline__ typename D::Vec sum_vec(const SumArgs& a,
     return pack8<D>(s);
 }
 
-// One element of the rank-order sum (same adds and roundings as sum_vec);
-// every rank's load is issued before the first add, so the element costs
-// one memory round trip rather than one per rank.
+// One element of the rank-order sum (same adds and roundings as sum_vec),
+// in two halves: every rank's load is issued first (load_elem), before the
+// thread's vector work, and added after it (fold_elem), so the element costs
+// no memory round trip of its own on the kernel's critical path (a loop of
+// load + add over the run-time rank count cost one per rank).
 template <class D, int RMAX>
-__device__ __forceinline__ float sum_elem(const SumArgs& a, uint64_t e)
+__device__ __forceinline__ void load_elem(const SumArgs& a, uint64_t e, float (&v)[RMAX])
 {
-    float v[RMAX];
 #pragma unroll
     for (int r = 0; r < RMAX; ++r)
         v[r] = r < a.R ? ld_elem<D>(a.in[r], e) : 0.0f;
+}
+
+template <class D, int RMAX>
+__device__ __forceinline__ float fold_elem(const SumArgs& a, const float (&v)[RMAX])
+{
     float s = v[0];
 #pragma unroll
     for (int r = 1; r < RMAX; ++r) {
@@ -145,7 +151,9 @@ __global__ void __launch_bounds__(256) vector_sum_kernel(const SumArgs a)
     const uint64_t tail = a.n - nvec * 8;
     if (tid < tail) {
         const uint64_t e = nvec * 8 + tid;
-        st_elem<D>(a.out, e, sum_elem<D, RMAX>(a, e));
+        float v[RMAX];
+        load_elem<D, RMAX>(a, e, v);
+        st_elem<D>(a.out, e, fold_elem<D, RMAX>(a, v));
     }
 }
 
@@ -201,7 +209,9 @@ __global__ void __launch_bounds__(256) vector_sum_wide_kernel(const SumArgs a)
     const uint64_t tail = a.n - n16 * 16;
     if (tid < tail) {
         const uint64_t e = n16 * 16 + tid;
-        st_elem<D>(a.out, e, sum_elem<D, RMAX>(a, e));
+        float v[RMAX];
+        load_elem<D, RMAX>(a, e, v);
+        st_elem<D>(a.out, e, fold_elem<D, RMAX>(a, v));
     }
 }
 
@@ -238,6 +248,19 @@ __global__ void __launch_bounds__(256) vector_sum_shift_kernel(const SumArgs a, 
     static_assert(D::bytes == 2, "16-bit elements");
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
     const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    // element by element: [0, h + 8) and [h + 8 * (nv - 1), n), element k by
+    // the grid's thread stride - 1 - k, which the launch leaves without
+    // vectors when the grid is not capped (so these elements add no memory
+    // round trip after a thread's vectors)
+    const uint64_t n_head = h + 8, tail0 = h + 8 * (nv - 1);
+    const uint64_t n_elem = n_head + (a.n - tail0);
+    if (tid + n_elem >= stride) {
+        const uint64_t k = stride - 1 - tid;
+        const uint64_t e = k < n_head ? k : tail0 + (k - n_head);
+        float ev[RMAX];
+        load_elem<D, RMAX>(a, e, ev);
+        st_elem<D>(a.out, e, fold_elem<D, RMAX>(a, ev));
+    }
     for (uint64_t j = 1 + tid; j + 1 < nv; j += stride) {
         const uint64_t off = 2 * (h + 8 * j);
         V raw[RMAX];
@@ -252,12 +275,6 @@ __global__ void __launch_bounds__(256) vector_sum_shift_kernel(const SumArgs a, 
             }
         }
         st_vec(a.out + off, sum_vec<D, RMAX>(a, raw));
-    }
-    // element by element: [0, h + 8) and [h + 8 * (nv - 1), n)
-    const uint64_t n_head = h + 8, tail0 = h + 8 * (nv - 1);
-    if (tid < n_head + (a.n - tail0)) {
-        const uint64_t e = tid < n_head ? tid : tail0 + (tid - n_head);
-        st_elem<D>(a.out, e, sum_elem<D, RMAX>(a, e));
     }
 }
 
@@ -337,7 +354,10 @@ static cudaError_t launch_t(const SumArgs& a, const LaunchCfg& c)
         const uint64_t nv = a.n > h ? (a.n - h) / 8 : 0;
         if (nv >= 3) {
             const void* fn = shift_fn<D>(rmax);
-            uint64_t blocks = (nv - 2 + threads - 1) / threads;
+            // vectors 1 .. nv-2, then the element-by-element head and tail
+            // (at most 8 + 15 elements) on threads of their own
+            const uint64_t n_elem = h + 8 + (a.n - (h + 8 * (nv - 1)));
+            uint64_t blocks = (nv - 2 + n_elem + threads - 1) / threads;
             const uint64_t cap = (uint64_t)c.sms * 8;
             if (blocks > cap)
                 blocks = cap;
