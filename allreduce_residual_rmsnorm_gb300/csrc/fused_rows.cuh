@@ -243,7 +243,9 @@ fused_rows_kernel(const FusedArgs a)
 
     __shared__ DF red[2][32];
     __shared__ float rstd_sh[2];
-    __shared__ DF part[2];          // this CTA's row partial, read by the cluster
+    // this CTA's row partial, read by the cluster as one 8-byte load
+    // (ld_dsmem_f2): DF alone is only 4-byte aligned
+    __shared__ __align__(8) DF part[2];
     int parity = 0;
     float amax_local = 0.0f;
 
