@@ -212,7 +212,8 @@ cudaError_t launch_fused_rows_t(int variant, const FusedArgs& a, const LaunchCfg
         // 64 registers: H=3072 86.3 -> 96.0), so they keep the plain kernel.
         bool ahead = false;
         if (D::bytes == 2 && C == 1 && rmax == 8 && Hv > 448 && Hv <= 512) {
-            if (a.R >= 6 && a.T > c.sms)
+            // the look-ahead instantiation carries no Lamport code
+            if (a.R >= 6 && a.T > c.sms && !a.lamport)
                 ahead = true;
             else if (a.T >= 2 * c.sms)
                 light = true;
