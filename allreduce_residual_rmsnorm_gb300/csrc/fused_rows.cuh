@@ -160,10 +160,14 @@ fused_rows_kernel(const FusedArgs a)
     }
     const unsigned C = CLUSTER ? cluster_size() : 1u;
 
-    // Lamport mode (run time); the look-ahead form for 6..8 ranks is launched
-    // in buffer mode only and carries no Lamport code (measured at R=8,
-    // T=8192, H=4096: 109.9 -> 106.2 us without it)
-#define AR_LAMPORT (AHEAD ? 0 : a.lamport)
+    // Lamport mode (run time).  The look-ahead form for 6..8 ranks and the
+    // two-rows-per-SM form for <= 4 ranks are launched in buffer mode only
+    // and carry no Lamport code (µs without it, T=8192, back-to-back /
+    // inputs evicted: R=8, H=4096 109.7 / 116.2 -> 106.0 / 109.7; R=3,
+    // H=4104 79.0 / 86.8 -> 71.2 / 79.8; R=2, H=6144 81.4 / 92.3 -> 79.0 /
+    // 88.8; R=3, H=5120 83.9 / 90.3 -> 86.4 / 86.5).  The two-rows form for
+    // 5 ranks keeps it (82.95 / 92.1 -> 85.5 / 95.8 without).
+#define AR_LAMPORT ((AHEAD || (LIGHT && VPT == 2)) ? 0 : a.lamport)
 
     // inputs and the slot state may be written by the preceding grid
     pdl_wait();

@@ -186,8 +186,9 @@ cudaError_t launch_fused_rows_t(int variant, const FusedArgs& a, const LaunchCfg
         // 105.8) and H=5632 (102.3 / 108.8 vs 101.6 / 112.7) split the two
         // timings and take the look-ahead.
         bool light = false;
+        // (buffer mode only: this instantiation carries no Lamport code)
         if (D::bytes == 2 && C == 1 && rmax <= 4 && Hv > 512 && Hv < 1024 &&
-            a.R * Hv <= 2304 && a.T >= 2 * c.sms) {
+            a.R * Hv <= 2304 && a.T >= 2 * c.sms && !a.lamport) {
             vpt = 2;
             light = true;
         }

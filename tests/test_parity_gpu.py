@@ -429,11 +429,12 @@ def test_lamport_wait_times_out_in_the_pipelined_row_and_reset_recovers():
 
 @pytest.mark.parametrize("R,T,H,dtype", [(4, 400, 4096, "bf16"), (2, 700, 8192, "fp16"),
                                          (3, 333, 2064, "bf16"), (8, 350, 4096, "bf16"),
-                                         (6, 200, 3728, "fp16")])
+                                         (6, 200, 3728, "fp16"), (3, 320, 5120, "bf16")])
 def test_forced_lamport_with_several_rows_per_block(R, T, H, dtype):
     """Lamport mode forced beyond the one-shot token count: every block runs
     several rows, so the look-ahead loads of the next row are polling loads
-    of the current slot."""
+    of the current slot (at shapes whose buffer-mode calls take a form
+    compiled without the Lamport code, the plain row kernel runs)."""
     w = W.FusedWorkload(f"lam_rows_{R}_{T}_{H}", R=R, T=T, H=H, dtype=dtype,
                         pattern=W.RES_NORM_NVFP4, seed=R + T)
     stats, _, _ = run_and_check(w, B.AR_VARIANT_CTA_ROW, staged=True, mode=B.AR_MODE_LAMPORT)
