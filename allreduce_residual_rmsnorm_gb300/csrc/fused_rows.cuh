@@ -103,7 +103,7 @@ __device__ __forceinline__ void fold_ranks(float (&s)[KCH][8],
 // spans its CTAs (a separate instantiation, so the common one-CTA-per-row
 // kernel carries none of the cluster code).
 template <class D, int RMAX, int VPT, bool WARP_ROW, bool CLUSTER = false, bool LIGHT = false,
-          bool AHEAD = false>
+          bool AHEAD = false, bool BUF = false>
 __global__ void __launch_bounds__(rows_max_threads<D, RMAX, VPT, WARP_ROW, LIGHT, AHEAD>(),
                                   rows_min_blocks<LIGHT>())
 fused_rows_kernel(const FusedArgs a)
@@ -129,6 +129,8 @@ fused_rows_kernel(const FusedArgs a)
     static_assert(!AHEAD || (D::bytes == 2 && VPT == 1 && RMAX == 8 && !WARP_ROW && !CLUSTER &&
                              !LIGHT),
                   "look-ahead of 5..8 ranks: 16-bit, one vector per thread, <= 512 threads");
+    static_assert(!BUF || (VPT == 1 && !WARP_ROW && !CLUSTER && !LIGHT && !AHEAD),
+                  "buffer-mode instantiation: the one-vector row-block kernel");
     static_assert(VPT % KCH == 0, "batch must divide VPT");
     static_assert(RMAX % RB == 0, "rank batch must divide RMAX");
 
@@ -160,14 +162,15 @@ fused_rows_kernel(const FusedArgs a)
     }
     const unsigned C = CLUSTER ? cluster_size() : 1u;
 
-    // Lamport mode (run time).  The look-ahead form for 6..8 ranks and the
-    // two-rows-per-SM form for <= 4 ranks are launched in buffer mode only
-    // and carry no Lamport code (µs without it, T=8192, back-to-back /
-    // inputs evicted: R=8, H=4096 109.7 / 116.2 -> 106.0 / 109.7; R=3,
-    // H=4104 79.0 / 86.8 -> 71.2 / 79.8; R=2, H=6144 81.4 / 92.3 -> 79.0 /
-    // 88.8; R=3, H=5120 83.9 / 90.3 -> 86.4 / 86.5).  The two-rows form for
-    // 5 ranks keeps it (82.95 / 92.1 -> 85.5 / 95.8 without).
-#define AR_LAMPORT ((AHEAD || (LIGHT && VPT == 2)) ? 0 : a.lamport)
+    // Lamport mode (run time).  The look-ahead form for 6..8 ranks, the
+    // two-rows-per-SM form for <= 4 ranks and the BUF instantiation are
+    // launched in buffer mode only and carry no Lamport code (µs without it,
+    // T=8192, back-to-back / inputs evicted: R=8, H=4096 109.7 / 116.2 ->
+    // 106.0 / 109.7; R=3, H=4104 79.0 / 86.8 -> 71.2 / 79.8; R=2, H=6144
+    // 81.4 / 92.3 -> 79.0 / 88.8; R=3, H=5120 83.9 / 90.3 -> 86.4 / 86.5).
+    // The two-rows form for 5 ranks keeps it (82.95 / 92.1 -> 85.5 / 95.8
+    // without).
+#define AR_LAMPORT ((AHEAD || BUF || (LIGHT && VPT == 2)) ? 0 : a.lamport)
 
     // inputs and the slot state may be written by the preceding grid
     pdl_wait();

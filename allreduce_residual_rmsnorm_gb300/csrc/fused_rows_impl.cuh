@@ -48,6 +48,19 @@ static const void* rows_light_fn(int rmax)
     return nullptr;
 }
 
+// one vector per thread, one row per block, buffer mode only (no Lamport code)
+template <class D>
+static const void* rows_buf_fn(int rmax)
+{
+    switch (rmax) {
+    case 2: return (const void*)fused_rows_kernel<D, 2, 1, false, false, false, false, true>;
+    case 4: return (const void*)fused_rows_kernel<D, 4, 1, false, false, false, false, true>;
+    case 8: return (const void*)fused_rows_kernel<D, 8, 1, false, false, false, false, true>;
+    case 16: return (const void*)fused_rows_kernel<D, 16, 1, false, false, false, false, true>;
+    default: return nullptr;
+    }
+}
+
 template <class D>
 static const void* rows_ahead_fn()
 {
@@ -234,8 +247,28 @@ cudaError_t launch_fused_rows_t(int variant, const FusedArgs& a, const LaunchCfg
             C = 1;
         threads = ((Hv + C * vpt - 1) / (C * vpt) + 31) / 32 * 32;
         if (C == 1) {
-            const int cap = c.sms * blocks_per_sm(fn, threads);
+            int cap = c.sms * blocks_per_sm(fn, threads);
             grid = a.T < cap ? a.T : cap;
+            // Few rows per block (decode-sized buffer calls, small prefills):
+            // the buffer-mode instantiation, whose kernel carries no Lamport
+            // code.  Measured (µs back-to-back, CUDA graphs with PDL; with
+            // the Lamport code -> without): R=4, H=8192 with FP8 output at
+            // T=256 / 512 / 1024 6.37 / 11.60 / 19.17 -> 5.84 / 10.45 / 18.87,
+            // but T=2048 39.5 -> 40.2; R=4, H=7168, T=384 8.30 -> 7.46; R=4,
+            // H=4096, T=512 5.55 -> 5.06; R=8, H=7168 with NVFP4 output at
+            // T=512 / 608 15.09 / 16.76 -> 14.65 / 15.98; R=8, T=8192 178.2 ->
+            // 179.2.  Hence 2..7 rows per block (with one row per block,
+            // R=8, T=128, H=4096, nothing gained: 2.98 µs either way).
+            if (vpt == 1 && !light && !ahead && !a.lamport) {
+                const void* fb = rows_buf_fn<D>(rmax);
+                const int capb = c.sms * blocks_per_sm(fb, threads);
+                const int gb = a.T < capb ? a.T : capb;
+                const int rpb = (a.T + gb - 1) / gb;
+                if (fb && rpb >= 2 && rpb <= 7) {
+                    fn = fb;
+                    grid = gb;
+                }
+            }
         } else {
             int ncl = max_clusters(fn, threads, C);
             if (ncl < 1)
