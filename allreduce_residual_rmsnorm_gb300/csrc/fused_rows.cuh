@@ -129,8 +129,8 @@ fused_rows_kernel(const FusedArgs a)
     static_assert(!AHEAD || (D::bytes == 2 && VPT == 1 && RMAX == 8 && !WARP_ROW && !CLUSTER &&
                              !LIGHT),
                   "look-ahead of 5..8 ranks: 16-bit, one vector per thread, <= 512 threads");
-    static_assert(!BUF || (VPT == 1 && !WARP_ROW && !CLUSTER && !LIGHT && !AHEAD),
-                  "buffer-mode instantiation: the one-vector row-block kernel");
+    static_assert(!BUF || (VPT <= 2 && !WARP_ROW && !CLUSTER && !LIGHT && !AHEAD),
+                  "buffer-mode instantiation: row-block kernels of one or two vectors");
     static_assert(VPT % KCH == 0, "batch must divide VPT");
     static_assert(RMAX % RB == 0, "rank batch must divide RMAX");
 

@@ -48,17 +48,24 @@ static const void* rows_light_fn(int rmax)
     return nullptr;
 }
 
-// one vector per thread, one row per block, buffer mode only (no Lamport code)
-template <class D>
-static const void* rows_buf_fn(int rmax)
+// one or two vectors per thread, one row per block, buffer mode only (no
+// Lamport code)
+template <class D, int VPT>
+static const void* rows_buf_fn_vpt(int rmax)
 {
     switch (rmax) {
-    case 2: return (const void*)fused_rows_kernel<D, 2, 1, false, false, false, false, true>;
-    case 4: return (const void*)fused_rows_kernel<D, 4, 1, false, false, false, false, true>;
-    case 8: return (const void*)fused_rows_kernel<D, 8, 1, false, false, false, false, true>;
-    case 16: return (const void*)fused_rows_kernel<D, 16, 1, false, false, false, false, true>;
+    case 2: return (const void*)fused_rows_kernel<D, 2, VPT, false, false, false, false, true>;
+    case 4: return (const void*)fused_rows_kernel<D, 4, VPT, false, false, false, false, true>;
+    case 8: return (const void*)fused_rows_kernel<D, 8, VPT, false, false, false, false, true>;
+    case 16: return (const void*)fused_rows_kernel<D, 16, VPT, false, false, false, false, true>;
     default: return nullptr;
     }
+}
+
+template <class D>
+static const void* rows_buf_fn(int rmax, int vpt)
+{
+    return vpt == 1 ? rows_buf_fn_vpt<D, 1>(rmax) : vpt == 2 ? rows_buf_fn_vpt<D, 2>(rmax) : nullptr;
 }
 
 template <class D>
@@ -258,9 +265,10 @@ cudaError_t launch_fused_rows_t(int variant, const FusedArgs& a, const LaunchCfg
             // H=4096, T=512 5.55 -> 5.06; R=8, H=7168 with NVFP4 output at
             // T=512 / 608 15.09 / 16.76 -> 14.65 / 15.98; R=8, T=8192 178.2 ->
             // 179.2.  Hence 2..7 rows per block (with one row per block,
-            // R=8, T=128, H=4096, nothing gained: 2.98 µs either way).
-            if (vpt == 1 && !light && !ahead && !a.lamport) {
-                const void* fb = rows_buf_fn<D>(rmax);
+            // R=8, T=128, H=4096, nothing gained: 2.98 µs either way).  Also
+            // for two vectors per thread: R=8, H=8192, T=256 7.49 -> 7.12.
+            if (vpt <= 2 && !light && !ahead && !a.lamport) {
+                const void* fb = rows_buf_fn<D>(rmax, vpt);
                 const int capb = c.sms * blocks_per_sm(fb, threads);
                 const int gb = a.T < capb ? a.T : capb;
                 const int rpb = (a.T + gb - 1) / gb;
